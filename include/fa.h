@@ -1,0 +1,111 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention forward library, libfa_gb300.so.
+ *
+ * The operation is the attention forward pass that the tile-programming guide
+ * ("Guia Prático de Programação de GPU com Tiles", section 6, flash attention) builds
+ * toward, with the FlashAttention-4 features named in "Como Domar o Blackwell Sem
+ * Enlouquecer com CUDA" (two MMA stages, online softmax, grouped-query attention):
+ *
+ *   for every batch b, query head h and query row i:
+ *     kvh       = h / (Hq / Hkv)                      (consecutive query heads share a KV head)
+ *     J         = { j < Sk : causal == 0  or  j <= i } (top-left causal alignment)
+ *     s_j       = scale * sum_d q[b,h,i,d] * k[b,kvh,j,d]
+ *     o[b,h,i,:]= sum_{j in J} exp(s_j - m) v[b,kvh,j,:] / sum_{j in J} exp(s_j - m),  m = max s_j
+ *     lse[b,h,i]= m + ln sum_{j in J} exp(s_j - m)    (natural log, float32)
+ *
+ * computed tile by tile with an online softmax; the Sq x Sk score matrix is never stored.
+ *
+ * Layout (all tensors dense, row-major, no strides in the ABI):
+ *   q   [B, Hq,  Sq, D]  16-bit (bf16 for fa_fwd, fp16 for fa_fwd_fp16)
+ *   k   [B, Hkv, Sk, D]  same type
+ *   v   [B, Hkv, Sk, D]  same type
+ *   o   [B, Hq,  Sq, D]  same type, round-to-nearest-even from the fp32 accumulator
+ *   lse [B, Hq,  Sq]     float32
+ *
+ * Ownership: every pointer is a DEVICE pointer on the current CUDA device, allocated and
+ * owned by the caller; the library allocates no device memory and keeps no pointer after
+ * the call returns.  o and lse must not overlap q, k, v or each other.
+ *
+ * Asynchrony: the kernel is enqueued on `stream` (0 = the legacy default stream) and the
+ * call returns without synchronising.  Argument errors are returned before any CUDA call
+ * is made.  The call never aborts, exits or traps; a device-side watchdog failure is
+ * reported later through fa_device_status().
+ *
+ * Thread safety: calls may be made from several host threads; the only shared mutable
+ * state is the per-device watchdog status word and read-only caches of device properties.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (binary-compatible with cudaStream_t / CUstream). */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL_PTR = 1,        /* q, k, v, o or lse is NULL for a non-empty problem        */
+    FA_ERR_BAD_DIM = 2,         /* B, Sq, Sk < 0, or Sk == 0 while B*Hq*Sq > 0, or too large */
+    FA_ERR_HEADS = 3,           /* Hq < 1, Hkv < 1, or Hq % Hkv != 0                         */
+    FA_ERR_UNSUPPORTED_D = 4,   /* D not in {64, 128}                                        */
+    FA_ERR_ALIGN = 5,           /* q/k/v/o not 16-byte aligned, or lse not 4-byte aligned    */
+    FA_ERR_ALIAS = 6,           /* o or lse overlaps an input or each other                  */
+    FA_ERR_SCALE = 7,           /* scale is NaN or infinite                                  */
+    FA_ERR_NO_DEVICE = 8,       /* no CUDA device / runtime error querying it                */
+    FA_ERR_ARCH = 9,            /* current device is not compute capability 10.3 (sm_103)    */
+    FA_ERR_TENSORMAP = 10,      /* cuTensorMapEncodeTiled unavailable or rejected the layout */
+    FA_ERR_LAUNCH = 11,         /* the kernel launch failed (cudaGetLastError)               */
+    FA_ERR_DEVICE_TIMEOUT = 12  /* (fa_device_status) a bounded device-side wait expired     */
+} fa_status_t;
+
+/*
+ * fa_fwd -- bf16 attention forward.  Writes o and lse as described above.
+ *   B, Hq, Hkv, Sq, Sk, D : sizes (D in {64, 128}; Hq % Hkv == 0)
+ *   causal                : 0 = full attention, nonzero = key j allowed only for j <= i
+ *   scale                 : multiplies q.k before the softmax (usually 1/sqrt(D))
+ *   stream                : CUDA stream to enqueue on
+ * B == 0 or Sq == 0 is a valid empty problem and returns FA_OK without touching memory.
+ * Returns FA_OK or one of the fa_status_t codes.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+           fa_stream_t stream);
+
+/* fa_fwd_fp16 -- identical to fa_fwd with IEEE fp16 q, k, v and o. */
+int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
+                int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                fa_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *fa_strerror(int status);
+
+/*
+ * fa_device_status -- synchronises `stream`, then reads and clears the current device's
+ * watchdog word.  Returns FA_OK if no kernel since the last read gave up on a wait,
+ * FA_ERR_DEVICE_TIMEOUT if one did (its CTAs then skipped the rest of their work and the
+ * outputs of that call are unspecified), or FA_ERR_NO_DEVICE on a CUDA error.
+ * *detail (if non-NULL) receives the raw word: bit 0 = timeout, bits 8..15 = the wait
+ * site that expired first.
+ */
+int fa_device_status(fa_stream_t stream, uint32_t *detail);
+
+/*
+ * fa_fwd_debug -- test hook: fa_fwd / fa_fwd_fp16 (is_fp16 selects) with an explicit
+ * watchdog limit per wait (timeout_ns, 0 = the default of 2 s) and a fault-injection mask
+ * (inject bit 0: the load warp skips the first V tile, so the MMA warp's wait for it
+ * expires; the kernel then records FA_ERR_DEVICE_TIMEOUT and every CTA returns normally).
+ * With inject == 0 and timeout_ns == 0 it is exactly fa_fwd / fa_fwd_fp16.
+ */
+int fa_fwd_debug(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                 fa_stream_t stream, int is_fp16, uint64_t timeout_ns, uint32_t inject);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

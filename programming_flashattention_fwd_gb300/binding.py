@@ -1,0 +1,151 @@
+"""ctypes binding of libfa_gb300.so -- argument marshalling only.
+
+Every step of the attention computation runs in the library's CUDA kernel; this module
+only turns torch tensors into device pointers, sizes and a stream handle, and raises
+FaError on a non-zero status.  The library must exist (built by ``build.build()``); a
+missing library raises at the first call -- there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+STATUS = {
+    0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_BAD_DIM", 3: "FA_ERR_HEADS",
+    4: "FA_ERR_UNSUPPORTED_D", 5: "FA_ERR_ALIGN", 6: "FA_ERR_ALIAS", 7: "FA_ERR_SCALE",
+    8: "FA_ERR_NO_DEVICE", 9: "FA_ERR_ARCH", 10: "FA_ERR_TENSORMAP", 11: "FA_ERR_LAUNCH",
+    12: "FA_ERR_DEVICE_TIMEOUT",
+}
+
+_lib = None
+_lock = threading.Lock()
+
+_FWD_ARGS = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_void_p]
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    for name in ("fa_fwd", "fa_fwd_fp16"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = _FWD_ARGS
+    lib.fa_fwd_debug.restype = ctypes.c_int
+    lib.fa_fwd_debug.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
+    lib.fa_strerror.restype = ctypes.c_char_p
+    lib.fa_strerror.argtypes = [ctypes.c_int]
+    lib.fa_device_status.restype = ctypes.c_int
+    lib.fa_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    return lib
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (once) and return the CUDA library; raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and (path is None or path == LIB_PATH):
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise FaError(-1, f"CUDA library not built: {p} is missing "
+                              "(run programming_flashattention_fwd_gb300.build.build())")
+        lib = _declare(ctypes.CDLL(p))
+        if p == LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def fa_strerror(status: int) -> str:
+    return load_library().fa_strerror(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check_tensors(q, k, v, o, lse):
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous ([B, H, S, D] dense layout)")
+        if t.numel() and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or o.dim() != 4 or lse.dim() != 3:
+        raise ValueError("q, k, v, o must be 4-D [B, H, S, D] and lse 3-D [B, Hq, Sq]")
+    if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("k and v must be [B, Hkv, Sk, D] with q's B and D")
+    if o.shape != q.shape or tuple(lse.shape) != tuple(q.shape[:3]):
+        raise ValueError("o must match q's shape and lse must be [B, Hq, Sq]")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype) or lse.dtype != torch.float32:
+        raise ValueError("q, k, v, o share one 16-bit dtype; lse is float32")
+
+
+def _call(fn_name: str, q, k, v, o, lse, causal: bool, scale: float, stream, extra=()):
+    _check_tensors(q, k, v, o, lse)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    lib = load_library()
+    st = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+                               _stream_handle(stream), *extra)
+    if st != 0:
+        raise FaError(st, fa_strerror(st))
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """bf16 attention forward into caller-allocated o [B,Hq,Sq,D] and lse [B,Hq,Sq] fp32."""
+    if q.dtype != torch.bfloat16:
+        raise ValueError("fa_fwd takes bf16 tensors (use fa_fwd_fp16 for fp16)")
+    _call("fa_fwd", q, k, v, o, lse, causal, scale, stream)
+
+
+def fa_fwd_fp16(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """fp16 attention forward into caller-allocated o and lse."""
+    if q.dtype != torch.float16:
+        raise ValueError("fa_fwd_fp16 takes fp16 tensors")
+    _call("fa_fwd_fp16", q, k, v, o, lse, causal, scale, stream)
+
+
+def fa_fwd_debug(q, k, v, o, lse, causal: bool, scale: float, timeout_ns: int = 0,
+                 inject: int = 0, stream=None) -> None:
+    """Test hook: the forward with an explicit watchdog limit and fault-injection mask."""
+    _call("fa_fwd_debug", q, k, v, o, lse, causal, scale, stream,
+          extra=(int(q.dtype == torch.float16), int(timeout_ns), int(inject)))
+
+
+def attention(q, k, v, causal: bool = False, scale: Optional[float] = None,
+              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Allocate o and lse on q's device and run the forward; returns (o, lse)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if q.dtype == torch.float16:
+        fa_fwd_fp16(q, k, v, o, lse, causal, scale, stream)
+    else:
+        fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def fa_device_status(stream=None) -> Tuple[int, int]:
+    """Synchronise the stream, read and clear the watchdog word: (status, raw word)."""
+    w = ctypes.c_uint32(0)
+    st = load_library().fa_device_status(_stream_handle(stream), ctypes.byref(w))
+    return int(st), int(w.value)

@@ -1,0 +1,178 @@
+// fa_api.cpp -- the C ABI declared in include/fa.h: argument validation (before any
+// CUDA call), device checks, TMA descriptor encoding and dispatch to the kernel.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn get_encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Per-device cache of "is this an sm_103 device": 0 unknown, 1 yes, 2 no.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_arch_ok[kMaxDevices];
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 3-D view (D, S, B*H) of a dense [B, H, S, D] 16-bit tensor; 64 x 128 x 1 boxes, 128B swizzle.
+bool encode(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, int D, int S, long long BH)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)fa::kBM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
+        int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject)
+{
+    // ---- argument checks: no CUDA call before these pass
+    if (B < 0 || Sq < 0 || Sk < 0) return FA_ERR_BAD_DIM;
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_HEADS;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+    if (!std::isfinite(scale)) return FA_ERR_SCALE;
+    if (B == 0 || Sq == 0) return FA_OK;
+    if (Sk == 0) return FA_ERR_BAD_DIM;
+    const long long BHq = (long long)B * Hq, BHkv = (long long)B * Hkv;
+    const long long Tq = (Sq + fa::kBM - 1) / fa::kBM, Tk = (Sk + fa::kBN - 1) / fa::kBN;
+    const long long NP = (Tq + 1) / 2;
+    if (BHq * NP > 0x7fffffffLL || BHq > 0x7fffffffLL) return FA_ERR_BAD_DIM;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return FA_ERR_ALIGN;
+    const size_t nq = (size_t)BHq * Sq * D * 2, nkv = (size_t)BHkv * Sk * D * 2, nl = (size_t)BHq * Sq * 4;
+    if (ranges_overlap(o, nq, q, nq) || ranges_overlap(o, nq, k, nkv) || ranges_overlap(o, nq, v, nkv) ||
+        ranges_overlap(lse, nl, q, nq) || ranges_overlap(lse, nl, k, nkv) || ranges_overlap(lse, nl, v, nkv) ||
+        ranges_overlap(lse, nl, o, nq))
+        return FA_ERR_ALIAS;
+
+    // ---- device
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
+    int st = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_NO_DEVICE;
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        g_arch_ok[dev].store(st, std::memory_order_relaxed);
+    }
+    if (st != 1) return FA_ERR_ARCH;
+
+    // ---- TMA descriptors
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return FA_ERR_TENSORMAP;
+    fa::Maps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode(enc, &maps.q, q, bf16, D, Sq, BHq) || !encode(enc, &maps.k, k, bf16, D, Sk, BHkv) ||
+        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv) || !encode(enc, &maps.o, o, bf16, D, Sq, BHq))
+        return FA_ERR_TENSORMAP;
+
+    fa::Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.Tq = (int)Tq;
+    p.Tk = (int)Tk;
+    p.NP = (int)NP;
+    p.group = Hq / Hkv;
+    p.num_units = (int)(BHq * NP);
+    p.sl2 = (float)((double)scale * 1.4426950408889634);
+    p.timeout_ns = timeout_ns;
+    p.inject = inject;
+
+    cudaError_t e = fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+} // namespace
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
+           int D, int causal, float scale, fa_stream_t stream)
+{
+    return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, true, 0, 0);
+}
+
+int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                int Sk, int D, int causal, float scale, fa_stream_t stream)
+{
+    return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, false, 0, 0);
+}
+
+int fa_fwd_debug(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                 int Sk, int D, int causal, float scale, fa_stream_t stream, int is_fp16, uint64_t timeout_ns,
+                 uint32_t inject)
+{
+    return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, is_fp16 == 0, timeout_ns, inject);
+}
+
+const char *fa_strerror(int status)
+{
+    switch (status) {
+    case FA_OK: return "FA_OK: success";
+    case FA_ERR_NULL_PTR: return "FA_ERR_NULL_PTR: a tensor pointer is NULL";
+    case FA_ERR_BAD_DIM: return "FA_ERR_BAD_DIM: negative size, Sk == 0 for a non-empty problem, or problem too large";
+    case FA_ERR_HEADS: return "FA_ERR_HEADS: Hq and Hkv must be >= 1 with Hq % Hkv == 0";
+    case FA_ERR_UNSUPPORTED_D: return "FA_ERR_UNSUPPORTED_D: head dimension D must be 64 or 128";
+    case FA_ERR_ALIGN: return "FA_ERR_ALIGN: q/k/v/o must be 16-byte aligned and lse 4-byte aligned";
+    case FA_ERR_ALIAS: return "FA_ERR_ALIAS: o or lse overlaps an input or each other";
+    case FA_ERR_SCALE: return "FA_ERR_SCALE: scale is NaN or infinite";
+    case FA_ERR_NO_DEVICE: return "FA_ERR_NO_DEVICE: no usable CUDA device";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not sm_103 (GB300)";
+    case FA_ERR_TENSORMAP: return "FA_ERR_TENSORMAP: TMA descriptor encoding failed";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a bounded device-side wait expired";
+    default: return "unknown fa status code";
+    }
+}
+
+int fa_device_status(fa_stream_t stream, uint32_t *detail)
+{
+    uint32_t w = 0;
+    if (fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &w) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    if (detail) *detail = w;
+    return (w & 1u) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,38 @@
+// fa_internal.h -- declarations shared by the host API (fa_api.cpp) and the kernel
+// translation unit (fa_fwd_sm103.cu).  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Tile sizes: 128 query rows x 128 keys per step (the guide's default block of 128).
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+
+// Per-launch scalar parameters (passed by value to the kernel).
+struct Params {
+    float *lse;         // [B, Hq, Sq] fp32
+    int B, Hq, Hkv, Sq, Sk;
+    int Tq, Tk;         // number of 128-row query / key tiles
+    int NP;             // query-tile pairs per (b, hq): ceil(Tq / 2)
+    int group;          // Hq / Hkv
+    int num_units;      // work units (query-tile pairs) in the whole problem: B * Hq * NP
+    float sl2;          // scale * log2(e): the exp2-domain multiplier of q.k
+    uint64_t timeout_ns;// watchdog limit of each bounded wait
+    uint32_t inject;    // fault-injection mask (0 in normal use)
+};
+
+// The four TMA descriptors: q, k, v, o as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.
+struct Maps {
+    CUtensorMap q, k, v, o;
+};
+
+// Launches the forward kernel for (D, dtype, causal).  Returns the cudaGetLastError() of the launch.
+cudaError_t launch_fwd(int D, bool bf16, bool causal, const Maps &maps, const Params &p, cudaStream_t stream);
+
+// Reads and clears the current device's watchdog word (synchronous on `stream`).
+cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word);
+
+} // namespace fa

@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads, exports every function include/fa.h declares, and
+rejects bad arguments with the documented status code before making any CUDA call.
+
+Every call in this file is rejected by validation (or is an empty problem), so none of
+them reaches the CUDA runtime: they are safe on machines with or without a GPU."""
+import math
+import os
+import re
+
+import pytest
+
+from programming_flashattention_fwd_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = fa_build.build()
+    from programming_flashattention_fwd_gb300 import binding
+    return binding.load_library(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def declared_status_codes():
+    text = open(HEADER).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(FA_\w+)\s*=\s*(\d+)", text)}
+
+
+def test_header_declares_the_entry_points():
+    fns = declared_functions()
+    for name in ("fa_fwd", "fa_fwd_fp16", "fa_strerror", "fa_device_status", "fa_fwd_debug"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/fa.h but not exported"
+
+
+def test_strerror_covers_every_code(lib):
+    codes = declared_status_codes()
+    assert len(codes) == 13 and sorted(codes.values()) == list(range(13))
+    msgs = set()
+    for name, val in codes.items():
+        msg = lib.fa_strerror(val).decode()
+        assert msg.startswith(name), (name, msg)
+        msgs.add(msg)
+    assert len(msgs) == len(codes)
+    assert lib.fa_strerror(999).decode() == "unknown fa status code"
+
+
+# Fake, 16-byte aligned, non-overlapping "device" addresses: validation never dereferences them.
+Q, K, V, O, L = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+GOOD = dict(B=1, Hq=4, Hkv=2, Sq=256, Sk=256, D=128, causal=1, scale=0.125)
+
+
+def call(lib, fn="fa_fwd", q=Q, k=K, v=V, o=O, lse=L, **over):
+    a = dict(GOOD, **over)
+    return getattr(lib, fn)(q, k, v, o, lse, a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["D"],
+                            a["causal"], a["scale"], None)
+
+
+@pytest.mark.parametrize("fn", ["fa_fwd", "fa_fwd_fp16"])
+@pytest.mark.parametrize("over,code", [
+    (dict(B=-1), 2), (dict(Sq=-5), 2), (dict(Sk=-1), 2), (dict(Sk=0), 2),
+    (dict(Hq=0), 3), (dict(Hkv=0), 3), (dict(Hq=6, Hkv=4), 3), (dict(Hq=2, Hkv=4), 3),
+    (dict(D=32), 4), (dict(D=96), 4), (dict(D=256), 4),
+    (dict(scale=math.nan), 7), (dict(scale=math.inf), 7),
+    (dict(B=100000, Hq=100000, Hkv=1), 2),
+])
+def test_invalid_arguments(lib, fn, over, code):
+    assert call(lib, fn, **over) == code
+
+
+def test_empty_problems_are_noops(lib):
+    # B == 0 or Sq == 0 returns FA_OK without touching memory, even with NULL pointers
+    assert call(lib, q=None, k=None, v=None, o=None, lse=None, B=0) == 0
+    assert call(lib, q=None, k=None, v=None, o=None, lse=None, Sq=0) == 0
+    assert call(lib, Sq=0, Sk=0) == 0
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_null_pointers(lib, which):
+    assert call(lib, **{which: None}) == 1
+
+
+@pytest.mark.parametrize("which,addr", [("q", Q + 8), ("k", K + 2), ("v", V + 4), ("o", O + 8), ("lse", L + 2)])
+def test_misaligned_pointers(lib, which, addr):
+    assert call(lib, **{which: addr}) == 5
+
+
+def test_lse_needs_only_4_byte_alignment(lib):
+    # A 4-byte aligned lse passes the alignment check and is then rejected by the overlap
+    # check (it sits inside o), so the call never reaches the CUDA runtime.
+    assert call(lib, lse=O + 4) == 6
+
+
+@pytest.mark.parametrize("over", [dict(o=Q), dict(o=K + 64), dict(lse=V), dict(lse=O + 16)])
+def test_overlapping_outputs(lib, over):
+    assert call(lib, **over) == 6
+
+
+def test_debug_entry_point_validates_the_same_way(lib):
+    f = lib.fa_fwd_debug
+    assert f(Q, K, V, O, L, 1, 3, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0) == 3
+    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 80, 0, 1.0, None, 1, 0, 0) == 4
