@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward pass on GB300 -- one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one fa_fwd call over the whole workload (every query row of every head and batch).
+``value`` is attention TFLOP/s (4*B*Hq*Sq*Sk*D, halved when causal) over the K timed steps,
+timed with CUDA events on the launching stream with the inputs resident in HBM; the L2 is
+flushed (a 256 MiB write) between timed steps, outside the events.  ``e2e`` is the same
+metric through the public Python binding with pinned host buffers: every step copies q, k, v
+host->device, runs the call and copies o and lse back, all inside the events.
+
+``roofline`` compares the kernel against the measured dense bf16 tensor peak of the pool's
+GB300s (MEASURED_PEAKS.json when present, else the fallback figure, as stated in the line).
+``cpu_baseline`` times the float64 CPU oracle on a bounded sample of the same workload's
+query rows, on all host cores.
+
+``--impl reference`` times that oracle instead (the reference arm: there is no other
+implementation of these pages to run): each step evaluates a bounded sample of query rows.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own replica of the workload
+(independent inputs, no collective on the data path); timings are max-reduced across ranks
+and ``value`` counts the work of all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak (causal / non-causal)"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_source_hash() -> str:
+    """sha256 of the CUDA sources: ties an ncu traffic figure to the kernel it measured."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "programming_flashattention_fwd_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary for this workload and this exact
+    kernel source (a line 'traffic_bytes_per_launch: N' next to 'kernel_source_sha: H'),
+    else None."""
+    want = kernel_source_hash()
+    for p in sorted(glob.glob(PROFILE_GLOB)):
+        txt = open(p).read()
+        if f"workload: {workload}" not in txt or f"kernel_source_sha: {want}" not in txt:
+            continue
+        for line in txt.splitlines():
+            if line.strip().startswith("traffic_bytes_per_launch:"):
+                try:
+                    return float(line.split(":", 1)[1])
+                except ValueError:
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in a background process."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self._th = threading.Thread(target=self._read, daemon=True)
+        self._th.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        where = "during timed region"
+        if not inside and rows:
+            inside = sorted(rows, key=lambda r: abs(r[0] - self.t1))[:3]
+            where = "nearest samples to the timed region (region shorter than the sampling period)"
+        if not inside:
+            return None
+        sm = sorted(float(r[1][2]) for r in inside if r[1][2].replace(".", "").isdigit())
+        mx = [float(r[1][3]) for r in inside if r[1][3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[1][6 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "where": where}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one process)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_row_flops(w, rows) -> float:
+    """4 * |allowed keys| * D floating-point operations per evaluated query row."""
+    i = rows[:, 2]
+    n = (i + 1).clip(max=w.Sk) if w.causal else i * 0 + w.Sk
+    return float(4.0 * n.sum() * w.D)
+
+
+def time_oracle(w, q, k, v, target_s: float, seed: int):
+    """Time the oracle on a seeded row sample sized to take about target_s seconds."""
+    import numpy as np
+    import oracle
+    from programming_flashattention_fwd_gb300.inputs import sample_rows
+    orc = oracle.load()
+    cores = orc.max_threads()
+    probe = sample_rows(w, n=max(cores * 4, 64), seed=seed, edge=False)
+    t0 = time.perf_counter()
+    orc.rows(q, k, v, w.is_fp16, w.causal, w.softmax_scale, probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(w.B * w.Hq * w.Sq, max(len(probe), len(probe) * target_s / dt)))
+    rows = sample_rows(w, n=n, seed=seed + 1, edge=False)
+    t0 = time.perf_counter()
+    orc.rows(q, k, v, w.is_fp16, w.causal, w.softmax_scale, rows)
+    dt = time.perf_counter() - t0
+    flops = oracle_row_flops(w, rows)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} seeded query rows of {w.name} (all heads/batches), "
+                      f"float64 C oracle with OpenMP, {dt:.1f} s",
+            "rows": int(len(rows)), "seconds": round(dt, 3)}
+
+
+def run_reference(args, w, world, rank):
+    """Reference arm: the float64 oracle, each step a bounded sample of query rows."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from programming_flashattention_fwd_gb300.inputs import make_qkv, sample_rows
+    q, k, v = make_qkv(w)
+    orc = oracle.load()
+    cores = orc.max_threads()
+    # size the per-step sample so that warmup + steps take about args.ref_seconds in total
+    probe = sample_rows(w, n=max(cores * 4, 64), seed=99, edge=False)
+    t0 = time.perf_counter()
+    orc.rows(q, k, v, w.is_fp16, w.causal, w.softmax_scale, probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    per_step_s = args.ref_seconds / max(1, args.steps + args.warmup)
+    n = int(min(w.B * w.Hq * w.Sq, max(len(probe), len(probe) * per_step_s / dt)))
+    flops_total, t_total = 0.0, 0.0
+    for s in range(args.warmup + args.steps):
+        rows = sample_rows(w, n=n, seed=1000 + s, edge=False)
+        t0 = time.perf_counter()
+        orc.rows(q, k, v, w.is_fp16, w.causal, w.softmax_scale, rows)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            flops_total += oracle_row_flops(w, rows)
+            t_total += dt
+    value = flops_total / t_total / 1e12
+    sample = f"{n} seeded query rows of {w.name} per step, float64 C oracle with OpenMP"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, args):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+            "dtype": w.dtype, "causal": w.causal, "scale": w.softmax_scale, "seed": w.seed,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, w, world, rank, local):
+    import numpy as np
+    import torch
+    from programming_flashattention_fwd_gb300 import binding
+    from programming_flashattention_fwd_gb300.inputs import make_qkv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    wr = w.with_(seed=w.seed + 7919 * rank) if rank else w     # independent replica per rank
+    q_h, k_h, v_h = make_qkv(wr)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    fn = binding.fa_fwd_fp16 if w.is_fp16 else binding.fa_fwd
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        fn(q, k, v, o, lse, w.causal, w.softmax_scale)
+    torch.cuda.synchronize(dev)
+    st, word = binding.fa_device_status()
+    if st != 0:
+        raise RuntimeError(f"device watchdog fired during warm-up (word {word:#x})")
+
+    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark("start")
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        fn(q, k, v, o, lse, w.causal, w.softmax_scale)
+        ends[s].record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark("end")
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    times = [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
+    t_step = max_over_ranks(sum(times) / len(times), world)
+    st, word = binding.fa_device_status()
+    if st != 0:
+        raise RuntimeError(f"device watchdog fired during the timed steps (word {word:#x})")
+
+    # ---- end to end through the public binding, pinned host buffers, copies inside the events
+    q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    o_p = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
+    l_p = torch.empty(q_h.shape[:3], dtype=torch.float32).pin_memory()
+    q2, k2, v2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    o2 = torch.empty_like(o)
+    l2 = torch.empty_like(lse)
+
+    def e2e_step():
+        q2.copy_(q_p, non_blocking=True)
+        k2.copy_(k_p, non_blocking=True)
+        v2.copy_(v_p, non_blocking=True)
+        fn(q2, k2, v2, o2, l2, w.causal, w.softmax_scale)
+        o_p.copy_(o2, non_blocking=True)
+        l_p.copy_(l2, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, world)
+    assert torch.equal(o_p, o.cpu()) and torch.equal(l_p, lse.cpu()), "e2e result differs from the device run"
+    h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
+    d2h = o_p.numel() * o_p.element_size() + l_p.numel() * 4
+
+    if rank != 0:
+        return
+    flops = w.flops()
+    peak, peak_sus, peak_src = measured_peaks()
+    achieved = flops / t_step / 1e12
+    traffic = ncu_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": flops * world / t_step / 1e12, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(w, args),
+        "e2e": {"value": flops * world / t_e2e / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} dense bf16 (burst)" + (
+                         f"; sustained {peak_sus}" if peak_sus else ""),
+                     "kernel": "fa::fa_fwd_kernel"},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(w, q_h, k_h, v_h, args.cpu_seconds, seed=w.seed + 100)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    from programming_flashattention_fwd_gb300.inputs import DEFAULT_BENCH_WORKLOAD, WORKLOADS
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_BENCH_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--ref-seconds", type=float, default=90.0, help="reference-arm total budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_init()
+    if world != args.gpus and world > 1:
+        args.gpus = world
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -116,7 +116,11 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.NP = (int)NP;
     p.group = Hq / Hkv;
     p.num_units = (int)(BHq * NP);
-    p.sl2 = (float)((double)scale * 1.4426950408889634);
+    // The kernel masks keys with -inf scores and takes the row maximum before scaling, so it
+    // needs a positive multiplier: a negative scale negates the scores instead, and a zero
+    // scale replaces every score by 0 (uniform weights), both exactly.
+    p.smode = scale > 0.f ? 0u : (scale < 0.f ? 1u : 2u);
+    p.sl2 = scale == 0.f ? 1.0f : (float)(std::fabs((double)scale) * 1.4426950408889634);
     p.timeout_ns = timeout_ns;
     p.inject = inject;
 

@@ -33,6 +33,7 @@
 //
 // Every wait is bounded (watchdog): on expiry the kernel records a status word, raises
 // a CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM and returns.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cstdint>
@@ -321,6 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
 
+            if (p.smode == 1) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) s[c] = -s[c];
+            } else if (p.smode == 2) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) s[c] = 0.f;
+            }
+
             // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal).
             const int kbase = j * kBN;
             const bool tail = kbase + kBN > p.Sk;
@@ -434,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
@@ -445,8 +455,16 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
 {
     auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
     const int smem = Cfg<D>::BYTES;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> configured{0};   // bit d: attribute set on device d
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
     Params q = p;
     if (q.timeout_ns == 0) q.timeout_ns = kDefaultTimeoutNs;
     kern<<<p.num_units, kThreads, smem, stream>>>(m.q, m.k, m.v, m.o, q);

@@ -19,7 +19,8 @@ struct Params {
     int NP;             // query-tile pairs per (b, hq): ceil(Tq / 2)
     int group;          // Hq / Hkv
     int num_units;      // work units (query-tile pairs) in the whole problem: B * Hq * NP
-    float sl2;          // scale * log2(e): the exp2-domain multiplier of q.k
+    float sl2;          // |scale| * log2(e): the exp2-domain multiplier of the scores
+    uint32_t smode;     // 0: scale > 0; 1: scale < 0 (scores negated); 2: scale == 0 (scores zeroed)
     uint64_t timeout_ns;// watchdog limit of each bounded wait
     uint32_t inject;    // fault-injection mask (0 in normal use)
 };

@@ -1,0 +1,183 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (stated for bf16/fp16 outputs): max |O - O_ref| <= 2e-2, mean |O - O_ref| <= 2e-3,
+max |lse - lse_ref| <= 1e-3.  O_ref and lse_ref are the oracle's float64 values on the very
+same (rounded) inputs.
+
+  - the five named workloads at full size, in the launch configuration the benchmark times,
+    checked on 256 seeded rows plus deterministic edge rows (first/last rows of the first
+    tiles, the ragged last tile, first/last head and batch); every output row is checked
+    to have been written (outputs are NaN-poisoned before the call);
+  - a sweep of small shapes checked on every row: sequence lengths 1..513 (ragged tails,
+    single rows, single keys), Sq != Sk, GQA groups 1..8, D 64/128, bf16/fp16, causal on/off;
+  - guard canaries around every output buffer (no write outside o and lse);
+  - bitwise determinism and a non-default stream;
+  - the watchdog: an injected missing load makes the kernel give up, report
+    FA_ERR_DEVICE_TIMEOUT and return; the context stays usable.
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from programming_flashattention_fwd_gb300 import build as fa_build
+from programming_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, make_qkv, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa_build.build()
+    from programming_flashattention_fwd_gb300 import binding
+    binding.load_library()
+    return binding
+
+
+def run_gpu(fa, w: Workload, q, k, v, poison=True):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:3], dtype=torch.float32, device="cuda")
+    if poison:
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+    fn = fa.fa_fwd_fp16 if w.is_fp16 else fa.fa_fwd
+    fn(qd, kd, vd, o, lse, w.causal, w.softmax_scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, f"watchdog fired (word {word:#x})"
+    return o, lse
+
+
+def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    og = o_gpu.detach().double().cpu().numpy() if isinstance(o_gpu, torch.Tensor) else o_gpu
+    lg = lse_gpu.detach().double().cpu().numpy() if isinstance(lse_gpu, torch.Tensor) else lse_gpu
+    assert np.all(np.isfinite(og)), f"{what}: non-finite O"
+    assert np.all(np.isfinite(lg)), f"{what}: non-finite lse"
+    err = np.abs(og - o_ref)
+    lerr = np.abs(lg - lse_ref)
+    assert err.max() <= MAX_ABS, f"{what}: max |dO| = {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean |dO| = {err.mean():.3e}"
+    assert lerr.max() <= LSE_ABS, f"{what}: max |dlse| = {lerr.max():.3e}"
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_parity(fa, orc, name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w)
+    o, lse = run_gpu(fa, w, q, k, v)
+    assert torch.isfinite(o).all().item(), "some output rows were never written"
+    assert torch.isfinite(lse).all().item(), "some lse entries were never written"
+    rows = sample_rows(w, n=256)
+    o_ref, l_ref = orc.rows(q, k, v, w.is_fp16, w.causal, w.softmax_scale, rows)
+    oc, lc = o.cpu(), lse.cpu()
+    r = torch.from_numpy(rows)
+    check(oc[r[:, 0], r[:, 1], r[:, 2]], lc[r[:, 0], r[:, 1], r[:, 2]], o_ref, l_ref, name)
+
+
+SWEEP = []
+for D in (64, 128):
+    for (B, Hq, Hkv, Sq, Sk) in [(1, 1, 1, 1, 1), (1, 2, 1, 17, 17), (2, 4, 2, 127, 127),
+                                 (1, 2, 2, 128, 128), (1, 3, 3, 129, 129), (1, 8, 1, 255, 255),
+                                 (1, 2, 2, 256, 256), (1, 4, 2, 384, 200), (1, 2, 1, 200, 384),
+                                 (1, 2, 2, 513, 513), (2, 2, 2, 1, 300), (1, 2, 2, 300, 1)]:
+        for causal in (False, True):
+            SWEEP.append((B, Hq, Hkv, Sq, Sk, D, causal))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal", SWEEP)
+def test_shape_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
+    seed = zlib.crc32(repr((B, Hq, Hkv, Sq, Sk, D, causal, dtype)).encode()) % 100000
+    w = Workload("sweep", B, Hq, Hkv, Sq, Sk, D, dtype, causal, seed,
+                 q_std=2.0 if dtype == "fp16" else 1.0, k_std=2.0 if dtype == "fp16" else 1.0)
+    q, k, v = make_qkv(w)
+    o, lse = run_gpu(fa, w, q, k, v)
+    o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
+    check(o, lse, o_ref, l_ref, f"{w}")
+
+
+def test_scale_variants(fa, orc):
+    """Non-default scales, including 0 (uniform weights) and a negative one."""
+    for scale in (0.0, -0.3, 0.9):
+        w = Workload("scale", 1, 4, 2, 300, 300, 128, "bf16", True, 7, scale=scale)
+        q, k, v = make_qkv(w)
+        o, lse = run_gpu(fa, w, q, k, v)
+        o_ref, l_ref = orc.full(q, k, v, False, True, scale)
+        check(o, lse, o_ref, l_ref, f"scale={scale}")
+
+
+def test_canaries_untouched(fa):
+    """Writes stay inside o and lse: sentinels around both buffers survive the call."""
+    w = Workload("canary", 2, 4, 2, 333, 333, 128, "bf16", True, 11)
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    pad = 4096
+    n_o, n_l = q.numel(), q.shape[0] * q.shape[1] * q.shape[2]
+    obuf = torch.full((n_o + 2 * pad,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((n_l + 2 * pad,), -777.0, dtype=torch.float32, device="cuda")
+    o = obuf[pad:pad + n_o].view(q.shape)
+    lse = lbuf[pad:pad + n_l].view(q.shape[:3])
+    fa.fa_fwd(q, k, v, o, lse, True, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert (obuf[:pad] == 12345.0).all() and (obuf[pad + n_o:] == 12345.0).all()
+    assert (lbuf[:pad] == -777.0).all() and (lbuf[pad + n_l:] == -777.0).all()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_deterministic_and_side_stream(fa):
+    w = WORKLOADS["mha_causal_b4_h16_s1024_d64"]
+    q, k, v = make_qkv(w)
+    o1, l1 = run_gpu(fa, w, q, k, v)
+    o2, l2 = run_gpu(fa, w, q, k, v)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    s = torch.cuda.Stream()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        o3 = torch.empty_like(qd)
+        l3 = torch.empty(qd.shape[:3], dtype=torch.float32, device="cuda")
+        fa.fa_fwd(qd, kd, vd, o3, l3, True, w.softmax_scale, stream=s)
+    s.synchronize()
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_attention_convenience_matches(fa):
+    w = WORKLOADS["mha_b1_h2_s128_d64"]
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    o, lse = fa.attention(q, k, v, causal=False)
+    o2, l2 = run_gpu(fa, w, q.cpu(), k.cpu(), v.cpu())
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+def test_watchdog_reports_and_recovers(fa, orc):
+    """An injected missing V load makes the bounded waits expire: the call reports
+    FA_ERR_DEVICE_TIMEOUT through fa_device_status and the context stays usable."""
+    w = Workload("wd", 1, 2, 2, 256, 256, 64, "bf16", False, 5)
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    o = torch.zeros_like(q)
+    lse = torch.zeros(q.shape[:3], dtype=torch.float32, device="cuda")
+    fa.fa_fwd_debug(q, k, v, o, lse, False, w.softmax_scale, timeout_ns=20_000_000, inject=1)
+    st, word = fa.fa_device_status()
+    assert st == 12 and (word & 1) == 1, (st, word)
+    assert ((word >> 8) & 0xFF) != 0
+    # afterwards: a normal call is correct and the status word is clean
+    o2, l2 = run_gpu(fa, w, q.cpu(), k.cpu(), v.cpu())
+    o_ref, l_ref = orc.full(q.cpu(), k.cpu(), v.cpu(), False, False, w.softmax_scale)
+    check(o2, l2, o_ref, l_ref, "after watchdog")
+    assert fa.fa_device_status() == (0, 0)
+
+
+def test_errors_raise(fa):
+    q = torch.zeros(1, 3, 8, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 3, 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd(q, k, k, o, lse, False, 0.1)
+    assert e.value.status == 3
