@@ -100,11 +100,12 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     fa::Maps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (!encode(enc, &maps.q, q, bf16, D, Sq, BHq) || !encode(enc, &maps.k, k, bf16, D, Sk, BHkv) ||
-        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv) || !encode(enc, &maps.o, o, bf16, D, Sq, BHq))
+        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv))
         return FA_ERR_TENSORMAP;
 
     fa::Params p;
     std::memset(&p, 0, sizeof(p));
+    p.o = o;
     p.lse = lse;
     p.B = B;
     p.Hq = Hq;

@@ -9,30 +9,32 @@
 // -- two MMA stages (S = Q K^T and O += P V), online softmax, grouped-query attention,
 // TMA, tensor memory, warp specialisation -- are how it is mapped onto the hardware.
 //
-// One CTA owns a pair of query tiles (rows [256p, 256p+256) of one (b, hq)) that share
-// the key/value stream; while the softmax warps of one tile work, the tensor pipe runs
-// the other tile's MMAs.
+// Persistent CTAs (one per SM) walk a static list of work units; a unit is a pair of
+// 128-row query tiles ("a" = rows [256p, 256p+128), "b" = the next 128) of one (b, hq)
+// that share the key/value stream.  While the softmax warps of one tile work, the tensor
+// pipe runs the other tile's MMAs.
 //
-//   warp 0        TMA producer: Q tiles once, then K_j, V_j into a ring of smem slots
+//   warp 0        TMA producer of K_j, V_j into a ring of shared-memory slots
 //   warp 1        TMEM allocator + MMA issuer (one thread): S_x = Q_x K_j^T, O_x += P_x V_j
-//   warps 2-3     idle
-//   warps 4-7     softmax + correction + epilogue of query tile a (one thread per row)
-//   warps 8-11    the same for query tile b
+//   warp 2        TMA producer of query tiles into three rotating Q buffers
+//   warp 3        idle
+//   warps 4-7     softmax + correction + epilogue of tile a of every unit (one thread per row)
+//   warps 8-11    the same for tile b
 //
 // TMEM (512 columns x 128 lanes, lane = query row):
 //   S_a [0,128)  S_b [128,256)  fp32 scores; P (16-bit, two per column) overwrites
 //                               the first 64 columns of S in place
 //   O_a [256,256+D)  O_b [256+D,256+2D)  fp32 accumulators
 //
-// Differences from the guide's kernel: exp2 with scale*log2(e) folded into one FMA;
-// the rescale of O is lazy (only when the running max grows by more than 2^8, so the
-// unnormalised P stays <= 256, well inside bf16/fp16 range; O and l always share the
-// same stale max, so the result is unchanged); K/V tails and the causal diagonal are
-// masked only on the tiles that need it; fully masked causal tiles are skipped; the
-// log-sum-exp is written out.
+// Differences from the guide's kernel: exp2 with |scale|*log2(e) folded into one FMA; the
+// rescale of O is lazy (only when the running max grows by more than 2^8, so the
+// unnormalised P stays <= 256, well inside bf16/fp16 range; O and l always share the same
+// stale max, so the result is unchanged); K/V tails and the causal diagonal are masked only
+// on the tiles that need it; fully masked causal tiles are skipped; the log-sum-exp is
+// written out.
 //
-// Every wait is bounded (watchdog): on expiry the kernel records a status word, raises
-// a CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM and returns.
+// Every wait is bounded (watchdog): on expiry the kernel records a status word, raises a
+// CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM and returns.
 #include <atomic>
 #include <cfloat>
 #include <climits>
@@ -46,12 +48,16 @@ namespace fa {
 __device__ unsigned int g_fa_status;  // watchdog word: bit 0 = a wait expired, bits 8-15 = first site
 
 constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168;      // 65536 / 384, rounded down to the allocation granule
+constexpr uint32_t kRegsLoad = 88;    // warps 0-3 after setmaxnreg.dec
+constexpr uint32_t kRegsSoftmax = 208;// warps 4-11 after setmaxnreg.inc: 88*128 + 208*256 == 168*384
+static_assert(kRegsLoad * 128 + kRegsSoftmax * 256 == kRegsLaunch * kThreads, "register split");
 constexpr float kTau = 8.0f;          // lazy-rescale threshold in log2 units (factor 256)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 enum WaitSite : uint32_t {
     SITE_PROD_EMPTY = 1, SITE_MMA_Q = 2, SITE_MMA_FULL = 3, SITE_MMA_P = 4,
-    SITE_SM_S = 5, SITE_SM_O = 6, SITE_DRAIN = 7
+    SITE_SM_S = 5, SITE_SM_O = 6, SITE_DRAIN = 7, SITE_QFREE = 8
 };
 
 template <int D>
@@ -59,11 +65,12 @@ struct Cfg {
     static constexpr int TILE = kBM * D * 2;     // bytes of one 128-row, D-column 16-bit tile
     static constexpr int PANELS = D / 64;        // 64-column (128-byte) swizzle panels per tile
     static constexpr int PANEL = kBM * 128;      // bytes of one panel
-    static constexpr int NS = (D == 128) ? 5 : 8;// K/V ring slots
-    static constexpr int OFF_Q = 0;              // two Q tiles (also the O staging buffers)
-    static constexpr int OFF_RING = 2 * TILE;
+    static constexpr int NQ = 3;                 // rotating query-tile buffers
+    static constexpr int NS = (D == 128) ? 4 : 8;// K/V ring slots
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_RING = NQ * TILE;
     static constexpr int OFF_BAR = OFF_RING + NS * TILE;
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 1;
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
@@ -91,11 +98,45 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return false;
 }
 
+// One work unit, decoded identically by every role.
+struct Unit {
+    int zq, zkv;      // q/o head plane (b*Hq + hq) and k/v head plane (b*Hkv + kvh)
+    int tA, tB;       // query tile indices
+    bool hasB;
+    int nA, nB, n;    // key tiles for tile a, tile b, and their maximum
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long g = (long long)round * G + ((round & 1) ? (G - 1 - c) : c);   // snake order
+    if (g >= p.num_units) return false;
+    int bh, pr;
+    if (CAUSAL) {   // heaviest query-tile pairs first
+        const int nbh = p.B * p.Hq;
+        pr = p.NP - 1 - (int)(g / nbh);
+        bh = (int)(g % nbh);
+    } else {        // consecutive units share a head (and its K/V in L2)
+        bh = (int)(g / p.NP);
+        pr = (int)(g % p.NP);
+    }
+    const int b = bh / p.Hq, hq = bh % p.Hq;
+    u.zq = b * p.Hq + hq;
+    u.zkv = b * p.Hkv + hq / p.group;
+    u.tA = 2 * pr;
+    u.tB = 2 * pr + 1;
+    u.hasB = u.tB < p.Tq;
+    u.nA = CAUSAL ? min(p.Tk, u.tA + 1) : p.Tk;
+    u.nB = u.hasB ? (CAUSAL ? min(p.Tk, u.tB + 1) : p.Tk) : 0;
+    u.n = max(u.nA, u.nB);
+    return true;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const Params p)
+                  const __grid_constant__ CUtensorMap tmV, const Params p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -107,40 +148,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const uint32_t sQ0 = sb + C::OFF_Q, sQ1 = sb + C::OFF_Q + C::TILE;
+    const uint32_t sQ = sb + C::OFF_Q;
     const uint32_t sRing = sb + C::OFF_RING;
-    const uint32_t barQ = sb + C::OFF_BAR;
-    auto bar_full = [&](int s) { return sb + C::OFF_BAR + 8u * (1 + s); };
-    auto bar_empty = [&](int s) { return sb + C::OFF_BAR + 8u * (1 + C::NS + s); };
-    const uint32_t barS0 = sb + C::OFF_BAR + 8u * (1 + 2 * C::NS);
-    const uint32_t barP0 = barS0 + 16u;
-    const uint32_t barO0 = barS0 + 32u;
+    const uint32_t bar0 = sb + C::OFF_BAR;
+    auto bar_q = [&](int i) { return bar0 + 8u * i; };                       // Q buffer i loaded
+    auto bar_qfree = [&](int i) { return bar0 + 8u * (C::NQ + i); };         // Q buffer i no longer read
+    auto bar_full = [&](int s) { return bar0 + 8u * (2 * C::NQ + s); };
+    auto bar_empty = [&](int s) { return bar0 + 8u * (2 * C::NQ + C::NS + s); };
+    const uint32_t barS0 = bar0 + 8u * (2 * C::NQ + 2 * C::NS);   // S_x ready (x = 0, 1)
+    const uint32_t barP0 = barS0 + 16u;                            // P_x written
+    const uint32_t barO0 = barS0 + 32u;                            // O_x final for the unit
     const uint32_t barDone = barS0 + 48u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
-    // ---- work unit: (b, hq, pair of query tiles); causal units are ordered heaviest first
-    const int u = blockIdx.x;
-    int bh, pr;
-    if (CAUSAL) {
-        const int nbh = p.B * p.Hq;
-        pr = p.NP - 1 - u / nbh;
-        bh = u % nbh;
-    } else {
-        bh = u / p.NP;
-        pr = u % p.NP;
-    }
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    const int kvh = hq / p.group;
-    const int zq = b * p.Hq + hq, zkv = b * p.Hkv + kvh;
-    const int tA = 2 * pr, tB = 2 * pr + 1;
-    const bool hasB = tB < p.Tq;
-    const int nA = CAUSAL ? min(p.Tk, tA + 1) : p.Tk;
-    const int nB = hasB ? (CAUSAL ? min(p.Tk, tB + 1) : p.Tk) : 0;
-    const int n = max(nA, nB);
-
     if (threadIdx.x == 0) {
-        mbar_init(barQ, 1);
+        for (int i = 0; i < C::NQ; ++i) {
+            mbar_init(bar_q(i), 1);
+            mbar_init(bar_qfree(i), 1);
+        }
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
@@ -163,7 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
-        tma_prefetch_map(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -171,54 +196,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const uint64_t tmo = p.timeout_ns;
 
-    if (warp == 0) {
-        // ============================================================ TMA producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(barQ, (hasB ? 2u : 1u) * C::TILE);
-            for (int pn = 0; pn < C::PANELS; ++pn) {
-                tma_load_3d(sQ0 + pn * C::PANEL, &tmQ, pn * 64, tA * kBM, zq, barQ);
-                if (hasB) tma_load_3d(sQ1 + pn * C::PANEL, &tmQ, pn * 64, tB * kBM, zq, barQ);
-            }
-            const int skip = (p.inject & 1u) ? 1 : -1;   // ring use 1 = V_0
-            int armed = 0;                                // ring uses issued so far
+    if (warp < 4) {
+        regs_dec<kRegsLoad>();
+        if (warp == 0 && lane == 0) {
+            // ======================================================== K/V producer
+            const int skip = (p.inject & 1u) ? 1 : -1;   // ring use 1 = the first V tile
+            int use = 0;                                  // ring uses armed so far
             bool ok = true;
-            for (int j = 0; j < n && ok; ++j) {
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int use = 2 * j + kv;
-                    const int s = use % C::NS;
-                    if (!wait_bar(bar_empty(s), ((use / C::NS) & 1) ^ 1, abort_flag, tmo, SITE_PROD_EMPTY)) {
-                        ok = false;
-                        break;
+            Unit u;
+            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+                for (int j = 0; j < u.n && ok; ++j) {
+                    for (int kv = 0; kv < 2; ++kv, ++use) {
+                        const int s = use % C::NS;
+                        if (!wait_bar(bar_empty(s), ((use / C::NS) & 1) ^ 1, abort_flag, tmo, SITE_PROD_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        if (use == skip) continue;
+                        mbar_arrive_expect_tx(bar_full(s), C::TILE);
+                        const CUtensorMap *m = kv ? &tmV : &tmK;
+#pragma unroll
+                        for (int pn = 0; pn < C::PANELS; ++pn)
+                            tma_load_3d(sRing + s * C::TILE + pn * C::PANEL, m, pn * 64, j * kBN, u.zkv,
+                                        bar_full(s));
                     }
-                    armed = use + 1;
-                    if (use == skip) continue;
-                    mbar_arrive_expect_tx(bar_full(s), C::TILE);
-                    const CUtensorMap *m = kv ? &tmV : &tmK;
-                    for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d(sRing + s * C::TILE + pn * C::PANEL, m, pn * 64, j * kBN, zkv, bar_full(s));
                 }
             }
             // Drain: every load this thread armed has landed before the CTA may exit.
-            wait_bar(barQ, 0, abort_flag, tmo, SITE_DRAIN, false);
-            for (int use = max(0, armed - C::NS); use < armed; ++use)
-                if (use != skip)
-                    wait_bar(bar_full(use % C::NS), (use / C::NS) & 1, abort_flag, tmo, SITE_DRAIN, false);
-        }
-    } else if (warp == 1) {
-        // ============================================================ MMA issuer
-        if (lane == 0) {
+            for (int x = max(0, use - C::NS); x < use; ++x)
+                if (x != skip) wait_bar(bar_full(x % C::NS), (x / C::NS) & 1, abort_flag, tmo, SITE_DRAIN, false);
+        } else if (warp == 2 && lane == 0) {
+            // ======================================================== Q producer
+            int tau = 0;   // query tiles loaded so far (buffer tau % 3)
+            bool ok = true;
+            Unit u;
+            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+                for (int x = 0; x < (u.hasB ? 2 : 1); ++x) {
+                    const int buf = tau % C::NQ;
+                    if (tau >= C::NQ &&
+                        !wait_bar(bar_qfree(buf), ((tau / C::NQ) - 1) & 1, abort_flag, tmo, SITE_QFREE)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_q(buf), C::TILE);
+                    const int t = x ? u.tB : u.tA;
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_3d(sQ + buf * C::TILE + pn * C::PANEL, &tmQ, pn * 64, t * kBM, u.zq, bar_q(buf));
+                    ++tau;
+                }
+            }
+            for (int x = max(0, tau - C::NQ); x < tau; ++x)
+                wait_bar(bar_q(x % C::NQ), (x / C::NQ) & 1, abort_flag, tmo, SITE_DRAIN, false);
+        } else if (warp == 1 && lane == 0) {
+            // ======================================================== MMA issuer
             constexpr uint32_t idS = idesc_f16(BF16, kBM, kBN, false);
             constexpr uint32_t idPV = idesc_f16(BF16, kBM, D, true);
-            const uint32_t tS0 = tmem + C::COL_S0, tS1 = tmem + C::COL_S1;
-            const uint32_t tO0 = tmem + C::COL_O0, tO1 = tmem + C::COL_O1;
+            const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
+            const uint32_t tO[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
 
             // S = Q K^T: A = Q tile, B = K tile, both K-major (rows of D contiguous
             // elements) in 128B-swizzled 64-column panels; 16 columns per instruction.
-            auto issue_s = [&](uint32_t dS, uint32_t sQ, uint32_t sK) {
+            auto issue_s = [&](uint32_t dS, uint32_t sQt, uint32_t sK) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-                    mma_ss(dS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idS, kk > 0);
+                    mma_ss(dS, sdesc_sw128(sQt + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idS, kk > 0);
                 }
             };
             // O += P V: A = P from TMEM (16-bit pairs per column), B = V tile, MN-major
@@ -230,182 +273,212 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ts(dO, tP + kk * 8, sdesc_sw128(sV + kk * 2048, C::PANEL, 1024), idPV,
                            (first && kk == 0) ? 0u : 1u);
             };
-            auto slot_k = [&](int j) { return (2 * j) % C::NS; };
-            auto slot_v = [&](int j) { return (2 * j + 1) % C::NS; };
-            auto ph_k = [&](int j) { return (uint32_t)(((2 * j) / C::NS) & 1); };
-            auto ph_v = [&](int j) { return (uint32_t)(((2 * j + 1) / C::NS) & 1); };
 
-            bool ok = wait_bar(barQ, 0, abort_flag, tmo, SITE_MMA_Q) &&
-                      wait_bar(bar_full(slot_k(0)), ph_k(0), abort_flag, tmo, SITE_MMA_FULL);
-            if (ok) {
+            int use = 0;               // ring uses consumed (K_j = use, V_j = use + 1 within a step)
+            int tau = 0;               // query tiles consumed
+            uint32_t ks[2] = {0, 0};   // key steps done per tile slot (barS / barP phase)
+            bool ok = true;
+            Unit u;
+            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+                const int nt = u.hasB ? 2 : 1;
+                const int buf[2] = {tau % C::NQ, (tau + 1) % C::NQ};
+                for (int x = 0; x < nt && ok; ++x)
+                    ok = wait_bar(bar_q(buf[x]), ((tau + x) / C::NQ) & 1, abort_flag, tmo, SITE_MMA_Q);
+                tau += nt;
+                const int nk[2] = {u.nA, u.nB};
+                const int uK0 = use;
+                if (ok) ok = wait_bar(bar_full(uK0 % C::NS), (uK0 / C::NS) & 1, abort_flag, tmo, SITE_MMA_FULL);
+                if (!ok) break;
                 tc_fence_after();
-                issue_s(tS0, sQ0, sRing + slot_k(0) * C::TILE);
-                tc_commit(barS0);
-                if (nB > 0) {
-                    issue_s(tS1, sQ1, sRing + slot_k(0) * C::TILE);
-                    tc_commit(barS0 + 8);
+                for (int x = 0; x < nt; ++x) {
+                    issue_s(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE);
+                    tc_commit(barS0 + 8u * x);
+                    if (nk[x] == 1) tc_commit(bar_qfree(buf[x]));
                 }
-                tc_commit(bar_empty(slot_k(0)));
-            }
-            for (int j = 0; j < n && ok; ++j) {
-                const bool more = j + 1 < n;
-                if (!wait_bar(bar_full(slot_v(j)), ph_v(j), abort_flag, tmo, SITE_MMA_FULL)) break;
-                if (more && !wait_bar(bar_full(slot_k(j + 1)), ph_k(j + 1), abort_flag, tmo, SITE_MMA_FULL)) break;
-                const uint32_t sV = sRing + slot_v(j) * C::TILE;
-                const uint32_t sKn = more ? sRing + slot_k(j + 1) * C::TILE : 0u;
-                if (j < nA) {
-                    if (!wait_bar(barP0, j & 1, abort_flag, tmo, SITE_MMA_P)) break;
-                    tc_fence_after();
-                    issue_pv(tO0, tS0, sV, j == 0);
-                    if (j == nA - 1) tc_commit(barO0);
+                tc_commit(bar_empty(uK0 % C::NS));
+                for (int j = 0; j < u.n; ++j) {
+                    const bool more = j + 1 < u.n;
+                    const int uV = use + 1, uKn = use + 2;
+                    if (!wait_bar(bar_full(uV % C::NS), (uV / C::NS) & 1, abort_flag, tmo, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    if (more && !wait_bar(bar_full(uKn % C::NS), (uKn / C::NS) & 1, abort_flag, tmo, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sV = sRing + (uV % C::NS) * C::TILE;
+                    const uint32_t sKn = sRing + (uKn % C::NS) * C::TILE;
+                    for (int x = 0; x < nt; ++x) {
+                        if (j < nk[x]) {
+                            if (!wait_bar(barP0 + 8u * x, ks[x] & 1, abort_flag, tmo, SITE_MMA_P)) {
+                                ok = false;
+                                break;
+                            }
+                            ++ks[x];
+                            tc_fence_after();
+                            issue_pv(tO[x], tS[x], sV, j == 0);
+                            if (j == nk[x] - 1) tc_commit(barO0 + 8u * x);
+                        }
+                        if (x == nt - 1) tc_commit(bar_empty(uV % C::NS));
+                        if (j + 1 < nk[x]) {
+                            issue_s(tS[x], sQ + buf[x] * C::TILE, sKn);
+                            tc_commit(barS0 + 8u * x);
+                            if (j + 2 == nk[x]) tc_commit(bar_qfree(buf[x]));
+                        }
+                    }
+                    if (!ok) break;
+                    if (more) tc_commit(bar_empty(uKn % C::NS));
+                    use += 2;
                 }
-                if (j + 1 < nA) {
-                    issue_s(tS0, sQ0, sKn);
-                    tc_commit(barS0);
-                }
-                if (j < nB) {
-                    if (!wait_bar(barP0 + 8, j & 1, abort_flag, tmo, SITE_MMA_P)) break;
-                    tc_fence_after();
-                    issue_pv(tO1, tS1, sV, j == 0);
-                    if (j == nB - 1) tc_commit(barO0 + 8);
-                }
-                tc_commit(bar_empty(slot_v(j)));
-                if (j + 1 < nB) {
-                    issue_s(tS1, sQ1, sKn);
-                    tc_commit(barS0 + 8);
-                }
-                if (more) tc_commit(bar_empty(slot_k(j + 1)));
             }
             // Drain: every MMA this thread issued has completed before TMEM is freed.
             tc_commit(barDone);
             wait_bar(barDone, 0, abort_flag, tmo, SITE_DRAIN, false);
         }
-    } else if (warp >= 4) {
+    } else {
+        regs_inc<kRegsSoftmax>();
         // ============================================================ softmax / correction / epilogue
-        const int x = (warp - 4) >> 2;             // which query tile of the pair
+        const int x = (warp - 4) >> 2;             // tile slot: a (0) or b (1)
         const int r = threadIdx.x - 128 * (1 + x); // row within the tile == TMEM lane
-        const int t = x ? tB : tA;
-        const int nk = x ? nB : nA;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + (x ? C::COL_S1 : C::COL_S0);
         const uint32_t tO = tmem + lane_off + (x ? C::COL_O1 : C::COL_O0);
         const uint32_t barS = barS0 + 8u * x, barP = barP0 + 8u * x, barO = barO0 + 8u * x;
-        const int row = t * kBM + r;
         const float sl2 = p.sl2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        uint32_t ks = 0, uo = 0;
+        bool ok = true;
+        Unit u;
+        for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+            if (x == 1 && !u.hasB) continue;
+            const int t = x ? u.tB : u.tA;
+            const int nk = x ? u.nB : u.nA;
+            const int row = t * kBM + r;
 
-        float m_used = -INFINITY;  // running max in exp2 units (possibly stale by <= kTau)
-        float l = 0.f;             // running sum of p at m_used
-        bool ok = nk > 0;
-        for (int j = 0; j < nk && ok; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bar(barS, j & 1, abort_flag, tmo, SITE_SM_S));
-            if (!ok) break;
-            tc_fence_after();
+            float m_used = -INFINITY;  // running max in exp2 units (possibly stale by <= kTau)
+            float l = 0.f;             // running sum of p at m_used
+            for (int j = 0; j < nk; ++j) {
+                ok = __all_sync(0xffffffffu, wait_bar(barS, ks & 1, abort_flag, tmo, SITE_SM_S));
+                if (!ok) break;
+                ++ks;
+                tc_fence_after();
 
-            float s[kBN];
-            {
-                uint32_t v0[32], v1[32], v2[32], v3[32];
-                tmem_ld_x32(tS + 0, v0);
-                tmem_ld_x32(tS + 32, v1);
-                tmem_ld_x32(tS + 64, v2);
-                tmem_ld_x32(tS + 96, v3);
-                tmem_wait_ld();
-                reg_fence_x32(v0);
-                reg_fence_x32(v1);
-                reg_fence_x32(v2);
-                reg_fence_x32(v3);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    s[c] = __uint_as_float(v0[c]);
-                    s[32 + c] = __uint_as_float(v1[c]);
-                    s[64 + c] = __uint_as_float(v2[c]);
-                    s[96 + c] = __uint_as_float(v3[c]);
-                }
-            }
-
-            if (p.smode == 1) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) s[c] = -s[c];
-            } else if (p.smode == 2) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) s[c] = 0.f;
-            }
-
-            // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal).
-            const int kbase = j * kBN;
-            const bool tail = kbase + kBN > p.Sk;
-            const bool diag = CAUSAL && (kbase + kBN - 1 > t * kBM);
-            if (tail || diag) {
-                int lim = p.Sk - 1 - kbase;
-                if (CAUSAL) lim = min(lim, row - kbase);
-#pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (c > lim) s[c] = -INFINITY;
-            }
-
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-            for (int c = 4; c < kBN; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
-            }
-            const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
-
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_used = m_new;
-            } else if (m_new - m_used > kTau) {
-                alpha = ex2_approx(m_used - m_new);
-                l *= alpha;
-                m_used = m_new;
-                rescale = true;
-            }
-            // Lazy correction of O (this row's previous P V products are complete: the
-            // S MMA that produced this tile was issued after them).
-            if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t ov[32];
-                    tmem_ld_x32(tO + c, ov);
+                uint32_t sv[kBN];
+                {
+                    uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 0);
+                    uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32);
+                    uint32_t(&v2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 64);
+                    uint32_t(&v3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 96);
+                    tmem_ld_x32(tS + 0, v0);
+                    tmem_ld_x32(tS + 32, v1);
+                    tmem_ld_x32(tS + 64, v2);
+                    tmem_ld_x32(tS + 96, v3);
                     tmem_wait_ld();
-                    reg_fence_x32(ov);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st_x32(tO + c, ov);
+                    reg_fence_x32(v0);
+                    reg_fence_x32(v1);
+                    reg_fence_x32(v2);
+                    reg_fence_x32(v3);
                 }
-            }
+                float *s = reinterpret_cast<float *>(sv);
 
-            const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-            float ls0 = 0.f, ls1 = 0.f;
+                if (p.smode == 1) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
+                    for (int c = 0; c < kBN; ++c) s[c] = -s[c];
+                } else if (p.smode == 2) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[32 * c + 2 * e], sl2, -msub));
-                    const float p1 = ex2_approx(fmaf(s[32 * c + 2 * e + 1], sl2, -msub));
-                    ls0 += p0;
-                    ls1 += p1;
-                    pk[e] = pack2<BF16>(p0, p1);
+                    for (int c = 0; c < kBN; ++c) s[c] = 0.f;
                 }
-                tmem_st_x16(tS + 16 * c, pk);
-            }
-            l += ls0 + ls1;
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(barP);
-        }
 
-        // ---- epilogue: O / l -> 16-bit -> swizzled smem (the tile's Q buffer) -> TMA store
-        const uint32_t stage = x ? sQ1 : sQ0;
-        uint8_t *stage_ptr = smem + C::OFF_Q + x * C::TILE;
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(barO, 0, abort_flag, tmo, SITE_SM_O));
-        if (ok) {
+                // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal).
+                const int kbase = j * kBN;
+                const bool tail = kbase + kBN > p.Sk;
+                const bool diag = CAUSAL && (kbase + kBN - 1 > t * kBM);
+                if (tail || diag) {
+                    int lim = p.Sk - 1 - kbase;
+                    if (CAUSAL) lim = min(lim, row - kbase);
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (c > lim) s[c] = -INFINITY;
+                }
+
+                float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+                float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+                for (int c = 12; c < kBN; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+                }
+                const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_used = m_new;
+                } else if (m_new - m_used > kTau) {
+                    alpha = ex2_approx(m_used - m_new);
+                    l *= alpha;
+                    m_used = m_new;
+                    rescale = true;
+                }
+                // Lazy correction of O (this row's previous P V products are complete: the
+                // S MMA that produced this tile was issued after them).
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t ov[32];
+                        tmem_ld_x32(tO + c, ov);
+                        tmem_wait_ld();
+                        reg_fence_x32(ov);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float lo, hi;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2), lo, hi);
+                            ov[e] = __float_as_uint(lo);
+                            ov[e + 1] = __float_as_uint(hi);
+                        }
+                        tmem_st_x32(tO + c, ov);
+                    }
+                }
+
+                const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+                const uint64_t negm2 = f2_pack(-msub, -msub);
+                uint64_t lsum2 = f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int i = 32 * c + 2 * e;
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(s[i], s[i + 1]), sl2x2, negm2), t0, t1);
+                        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                        lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+                        pk[e] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st_x16(tS + 16 * c, pk);
+                }
+                float la, lb;
+                f2_unpack(lsum2, la, lb);
+                l += la + lb;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(barP);
+            }
+            if (!ok) break;
+
+            // ---- epilogue: O / l -> 16-bit -> global (one 2*D-byte row per thread), and lse
+            ok = __all_sync(0xffffffffu, wait_bar(barO, uo & 1, abort_flag, tmo, SITE_SM_O));
+            if (!ok) break;
+            ++uo;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const uint64_t il2 = f2_pack(inv_l, inv_l);
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)u.zq * p.Sq + row) * (size_t)(D * 2);
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t ov[32];
@@ -414,29 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence_x32(ov);
                 uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2<BF16>(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
-                const int panel = c >> 6;
-                const int chunk0 = (c & 63) >> 3;   // first 16-byte chunk of these 32 columns
+                for (int e = 0; e < 16; ++e) {
+                    float lo, hi;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), il2), lo, hi);
+                    pk[e] = pack2<BF16>(lo, hi);
+                }
+                if (row < p.Sq) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = (chunk0 + q4) ^ (r & 7);
-                    uint4 val = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                    *reinterpret_cast<uint4 *>(stage_ptr + panel * C::PANEL + r * 128 + chunk * 16) = val;
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        st_global_v4(orow + c * 2 + q4 * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
                 }
             }
             if (row < p.Sq) {
                 const float lse = l > 0.f ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
-                p.lse[(size_t)zq * p.Sq + row] = lse;
+                p.lse[(size_t)u.zq * p.Sq + row] = lse;
             }
-            fence_proxy_async_smem();
-        }
-        named_bar_sync(1 + x, 128);
-        if (r == 0 && nk > 0 && !*abort_flag) {
-            for (int pn = 0; pn < C::PANELS; ++pn)
-                tma_store_3d(&tmO, pn * 64, t * kBM, zq, stage + pn * C::PANEL);
-            tma_store_commit();
-            tma_store_wait_all();
         }
     }
 
@@ -455,19 +520,33 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
 {
     auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
     const int smem = Cfg<D>::BYTES;
-    static std::atomic<uint64_t> configured{0};   // bit d: attribute set on device d
+    // Per device: shared-memory opt-in, SM count, and a check that the compiled kernel
+    // really uses kRegsLaunch registers per thread -- the setmaxnreg split above adds up
+    // to exactly that launch allocation and could never be satisfied with less.
+    static std::atomic<uint64_t> configured{0};
+    static std::atomic<int> sm_count[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, kern);
+        if (e != cudaSuccess) return e;
+        if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidKernelImage;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        sm_count[dev].store(nsm, std::memory_order_relaxed);
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     Params q = p;
     if (q.timeout_ns == 0) q.timeout_ns = kDefaultTimeoutNs;
-    kern<<<p.num_units, kThreads, smem, stream>>>(m.q, m.k, m.v, m.o, q);
+    const int grid = min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
+    kern<<<grid, kThreads, smem, stream>>>(m.q, m.k, m.v, q);
     return cudaGetLastError();
 }
 

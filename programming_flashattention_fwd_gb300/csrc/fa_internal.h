@@ -13,6 +13,7 @@ constexpr int kBN = 128;
 
 // Per-launch scalar parameters (passed by value to the kernel).
 struct Params {
+    void *o;            // [B, Hq, Sq, D] 16-bit
     float *lse;         // [B, Hq, Sq] fp32
     int B, Hq, Hkv, Sq, Sk;
     int Tq, Tk;         // number of 128-row query / key tiles
@@ -25,9 +26,9 @@ struct Params {
     uint32_t inject;    // fault-injection mask (0 in normal use)
 };
 
-// The four TMA descriptors: q, k, v, o as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.
+// The TMA descriptors: q, k, v as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.
 struct Maps {
-    CUtensorMap q, k, v, o;
+    CUtensorMap q, k, v;
 };
 
 // Launches the forward kernel for (D, dtype, causal).  Returns the cudaGetLastError() of the launch.
