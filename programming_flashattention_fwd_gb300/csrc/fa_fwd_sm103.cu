@@ -70,7 +70,7 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * TILE;
     static constexpr int OFF_BAR = OFF_RING + NS * TILE;
-    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1;
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 4 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
@@ -156,9 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_full = [&](int s) { return bar0 + 8u * (2 * C::NQ + s); };
     auto bar_empty = [&](int s) { return bar0 + 8u * (2 * C::NQ + C::NS + s); };
     const uint32_t barS0 = bar0 + 8u * (2 * C::NQ + 2 * C::NS);   // S_x ready (x = 0, 1)
-    const uint32_t barP0 = barS0 + 16u;                            // P_x written
-    const uint32_t barO0 = barS0 + 32u;                            // O_x final for the unit
-    const uint32_t barDone = barS0 + 48u;
+    const uint32_t barP0 = barS0 + 16u;                            // P_x keys [64h, 64h+64) written: + 16x + 8h
+    const uint32_t barO0 = barS0 + 48u;                            // O_x final for the unit
+    const uint32_t barDone = barS0 + 64u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -173,8 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(barS0, 1);
         mbar_init(barS0 + 8, 1);
-        mbar_init(barP0, 4);
-        mbar_init(barP0 + 8, 4);
+        for (int i = 0; i < 4; ++i) mbar_init(barP0 + 8 * i, 4);
         mbar_init(barO0, 1);
         mbar_init(barO0 + 8, 1);
         mbar_init(barDone, 1);
@@ -248,30 +247,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int x = max(0, tau - C::NQ); x < tau; ++x)
                 wait_bar(bar_q(x % C::NQ), (x / C::NQ) & 1, abort_flag, tmo, SITE_DRAIN, false);
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ======================================================== MMA issuer
+            // The whole warp runs this loop in uniform control flow (so descriptors live in
+            // uniform registers); one elected lane issues each tcgen05 instruction.
             constexpr uint32_t idS = idesc_f16(BF16, kBM, kBN, false);
             constexpr uint32_t idPV = idesc_f16(BF16, kBM, D, true);
+            constexpr uint32_t HI = sdesc_hi_sw128(1024);   // 8-row groups 1024 bytes apart
             const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
             const uint32_t tO[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
+            auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) {
+                return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, tmo, site));
+            };
 
             // S = Q K^T: A = Q tile, B = K tile, both K-major (rows of D contiguous
             // elements) in 128B-swizzled 64-column panels; 16 columns per instruction.
             auto issue_s = [&](uint32_t dS, uint32_t sQt, uint32_t sK) {
+                const uint32_t qlo = sdesc_lo(sQt, 16), klo = sdesc_lo(sK, 16);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-                    mma_ss(dS, sdesc_sw128(sQt + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = (uint32_t)((kk >> 2) * C::PANEL + (kk & 3) * 32) >> 4;
+                    mma_ss_elect(dS, qlo + off, klo + off, HI, idS, kk > 0);
                 }
             };
-            // O += P V: A = P from TMEM (16-bit pairs per column), B = V tile, MN-major
-            // (D contiguous per key row): 8-key groups 1024 bytes apart, 64-column
-            // panels C::PANEL bytes apart; 16 keys per instruction.
-            auto issue_pv = [&](uint32_t dO, uint32_t tP, uint32_t sV, bool first) {
+            // O += P V for keys [64h, 64h+64): A = P from TMEM (16-bit pairs per column),
+            // B = V tile, MN-major (D contiguous per key row): 8-key groups 1024 bytes apart,
+            // 64-column panels C::PANEL bytes apart; 16 keys per instruction.
+            auto issue_pv_half = [&](uint32_t dO, uint32_t tP, uint32_t sV, int h, bool first) {
+                const uint32_t vlo = sdesc_lo(sV, C::PANEL);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(dO, tP + kk * 8, sdesc_sw128(sV + kk * 2048, C::PANEL, 1024), idPV,
-                           (first && kk == 0) ? 0u : 1u);
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int kk = 4 * h + k4;
+                    mma_ts_elect(dO, tP + kk * 8, vlo + (uint32_t)((kk * 2048) >> 4), HI, idPV,
+                                 (first && kk == 0) ? 0u : 1u);
+                }
             };
 
             int use = 0;               // ring uses consumed (K_j = use, V_j = use + 1 within a step)
@@ -283,27 +292,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nt = u.hasB ? 2 : 1;
                 const int buf[2] = {tau % C::NQ, (tau + 1) % C::NQ};
                 for (int x = 0; x < nt && ok; ++x)
-                    ok = wait_bar(bar_q(buf[x]), ((tau + x) / C::NQ) & 1, abort_flag, tmo, SITE_MMA_Q);
+                    ok = wait_u(bar_q(buf[x]), ((tau + x) / C::NQ) & 1, SITE_MMA_Q);
                 tau += nt;
                 const int nk[2] = {u.nA, u.nB};
                 const int uK0 = use;
-                if (ok) ok = wait_bar(bar_full(uK0 % C::NS), (uK0 / C::NS) & 1, abort_flag, tmo, SITE_MMA_FULL);
+                if (ok) ok = wait_u(bar_full(uK0 % C::NS), (uK0 / C::NS) & 1, SITE_MMA_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 for (int x = 0; x < nt; ++x) {
                     issue_s(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE);
-                    tc_commit(barS0 + 8u * x);
-                    if (nk[x] == 1) tc_commit(bar_qfree(buf[x]));
+                    tc_commit_elect(barS0 + 8u * x);
+                    if (nk[x] == 1) tc_commit_elect(bar_qfree(buf[x]));
                 }
-                tc_commit(bar_empty(uK0 % C::NS));
+                tc_commit_elect(bar_empty(uK0 % C::NS));
                 for (int j = 0; j < u.n; ++j) {
                     const bool more = j + 1 < u.n;
                     const int uV = use + 1, uKn = use + 2;
-                    if (!wait_bar(bar_full(uV % C::NS), (uV / C::NS) & 1, abort_flag, tmo, SITE_MMA_FULL)) {
+                    if (!wait_u(bar_full(uV % C::NS), (uV / C::NS) & 1, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
-                    if (more && !wait_bar(bar_full(uKn % C::NS), (uKn / C::NS) & 1, abort_flag, tmo, SITE_MMA_FULL)) {
+                    if (more && !wait_u(bar_full(uKn % C::NS), (uKn / C::NS) & 1, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -311,30 +320,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sKn = sRing + (uKn % C::NS) * C::TILE;
                     for (int x = 0; x < nt; ++x) {
                         if (j < nk[x]) {
-                            if (!wait_bar(barP0 + 8u * x, ks[x] & 1, abort_flag, tmo, SITE_MMA_P)) {
-                                ok = false;
-                                break;
+                            for (int h = 0; h < 2 && ok; ++h) {
+                                ok = wait_u(barP0 + 16u * x + 8u * h, ks[x] & 1, SITE_MMA_P);
+                                if (!ok) break;
+                                tc_fence_after();
+                                issue_pv_half(tO[x], tS[x], sV, h, j == 0);
                             }
+                            if (!ok) break;
                             ++ks[x];
-                            tc_fence_after();
-                            issue_pv(tO[x], tS[x], sV, j == 0);
-                            if (j == nk[x] - 1) tc_commit(barO0 + 8u * x);
+                            if (j == nk[x] - 1) tc_commit_elect(barO0 + 8u * x);
                         }
-                        if (x == nt - 1) tc_commit(bar_empty(uV % C::NS));
+                        if (x == nt - 1) tc_commit_elect(bar_empty(uV % C::NS));
                         if (j + 1 < nk[x]) {
                             issue_s(tS[x], sQ + buf[x] * C::TILE, sKn);
-                            tc_commit(barS0 + 8u * x);
-                            if (j + 2 == nk[x]) tc_commit(bar_qfree(buf[x]));
+                            tc_commit_elect(barS0 + 8u * x);
+                            if (j + 2 == nk[x]) tc_commit_elect(bar_qfree(buf[x]));
                         }
                     }
                     if (!ok) break;
-                    if (more) tc_commit(bar_empty(uKn % C::NS));
+                    if (more) tc_commit_elect(bar_empty(uKn % C::NS));
                     use += 2;
                 }
             }
-            // Drain: every MMA this thread issued has completed before TMEM is freed.
-            tc_commit(barDone);
+            // Drain: every MMA this warp issued has completed before TMEM is freed.
+            tc_commit_elect(barDone);
             wait_bar(barDone, 0, abort_flag, tmo, SITE_DRAIN, false);
+            __syncwarp();
         }
     } else {
         regs_inc<kRegsSoftmax>();
@@ -344,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + (x ? C::COL_S1 : C::COL_S0);
         const uint32_t tO = tmem + lane_off + (x ? C::COL_O1 : C::COL_O0);
-        const uint32_t barS = barS0 + 8u * x, barP = barP0 + 8u * x, barO = barO0 + 8u * x;
+        const uint32_t barS = barS0 + 8u * x, barP = barP0 + 16u * x, barO = barO0 + 8u * x;
         const float sl2 = p.sl2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t ks = 0, uo = 0;
@@ -447,9 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float msub = (m_used == -INFINITY) ? 0.f : m_used;
                 const uint64_t negm2 = f2_pack(-msub, -msub);
                 uint64_t lsum2 = f2_pack(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
+                // p = exp2(s*sl2 - m) for 32 keys -> 16 packed 16-bit pairs; l accumulates fp32 p.
+                auto exp_chunk = [&](int c, uint32_t(&pk)[16]) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int i = 32 * c + 2 * e;
@@ -459,15 +469,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lsum2 = f2_add(lsum2, f2_pack(p0, p1));
                         pk[e] = pack2<BF16>(p0, p1);
                     }
-                    tmem_st_x16(tS + 16 * c, pk);
+                };
+                // P goes out in two halves (keys 0-63, 64-127) so the MMA warp can start the
+                // first half of O += P V while the second half is still being exponentiated.
+                auto publish = [&](uint32_t bar) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar);
+                };
+                {
+                    uint32_t pk0[16], pk1[16], pk2[16], pk3[16];
+                    exp_chunk(0, pk0);
+                    tmem_st_x16(tS + 0, pk0);
+                    exp_chunk(1, pk1);
+                    tmem_st_x16(tS + 16, pk1);
+                    exp_chunk(2, pk2);
+                    publish(barP);
+                    tmem_st_x16(tS + 32, pk2);
+                    exp_chunk(3, pk3);
+                    tmem_st_x16(tS + 48, pk3);
+                    publish(barP + 8);
                 }
                 float la, lb;
                 f2_unpack(lsum2, la, lb);
                 l += la + lb;
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(barP);
             }
             if (!ok) break;
 

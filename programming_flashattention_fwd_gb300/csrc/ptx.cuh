@@ -292,4 +292,49 @@ __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, 
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// ---------------------------------------------------------------- elected-lane MMA issue
+// The whole warp executes these (uniform control flow, warp-uniform operands); elect.sync
+// picks one lane, which alone issues the instruction.  Descriptors are passed as their two
+// 32-bit halves: the low word carries the start address and leading offset, the high word
+// the stride offset, version and swizzle mode.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .b64 a, b;\n\t.reg .pred p, e;\n\t"
+                 "mov.b64 a, {%1, %3};\n\t"
+                 "mov.b64 b, {%2, %3};\n\t"
+                 "setp.ne.b32 p, %5, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .b64 b;\n\t.reg .pred p, e;\n\t"
+                 "mov.b64 b, {%2, %3};\n\t"
+                 "setp.ne.b32 p, %5, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+// Descriptor halves for 128B-swizzled operands (same field layout as sdesc_sw128).
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes)
+{
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo_bytes)
+{
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
 } // namespace fa
