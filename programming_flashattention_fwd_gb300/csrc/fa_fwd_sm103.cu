@@ -457,8 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 const float msub = (m_used == -INFINITY) ? 0.f : m_used;
                 const uint64_t negm2 = f2_pack(-msub, -msub);
-                uint64_t lsum2 = f2_pack(0.f, 0.f);
-                // p = exp2(s*sl2 - m) for 32 keys -> 16 packed 16-bit pairs; l accumulates fp32 p.
+                // p = exp2(s*sl2 - m) for 32 keys -> 16 packed 16-bit pairs; l accumulates fp32 p
+                // in eight independent packed partial sums (no long dependent add chain).
+                uint64_t lsum2[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lsum2[i] = f2_pack(0.f, 0.f);
                 auto exp_chunk = [&](int c, uint32_t(&pk)[16]) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float t0, t1;
                         f2_unpack(f2_fma(f2_pack(s[i], s[i + 1]), sl2x2, negm2), t0, t1);
                         const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-                        lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+                        lsum2[e & 7] = f2_add(lsum2[e & 7], f2_pack(p0, p1));
                         pk[e] = pack2<BF16>(p0, p1);
                     }
                 };
@@ -491,8 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_x16(tS + 48, pk3);
                     publish(barP + 8);
                 }
+                const uint64_t q0 = f2_add(f2_add(lsum2[0], lsum2[1]), f2_add(lsum2[2], lsum2[3]));
+                const uint64_t q1 = f2_add(f2_add(lsum2[4], lsum2[5]), f2_add(lsum2[6], lsum2[7]));
                 float la, lb;
-                f2_unpack(lsum2, la, lb);
+                f2_unpack(f2_add(q0, q1), la, lb);
                 l += la + lb;
             }
             if (!ok) break;
