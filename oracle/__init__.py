@@ -11,7 +11,9 @@ the passages it follows, is documented at the top of ``fa_oracle.c``:
     o[b,h,i,:] = sum_j softmax_j(scale * q[b,h,i,:] . k[b,h/g,j,:]) * v[b,h/g,j,:]
     lse[b,h,i] = ln sum_j exp(scale * q . k_j)          (natural log)
 
-over the allowed keys j < Sk (and j <= i when causal), with g = Hq / Hkv.
+over the allowed keys j < Sk -- and j <= i when causal == 1 (top-left), j <= i + Sk - Sq when
+causal == 2 (bottom-right) -- with g = Hq / Hkv.  A row with no allowed key gets o = 0 and
+lse = -inf.
 """
 from __future__ import annotations
 
@@ -75,9 +77,11 @@ class Oracle:
     def decode(self, bits: int, is_fp16: bool) -> float:
         return float(self.lib.fa_oracle_decode(int(bits) & 0xFFFF, int(bool(is_fp16))))
 
-    def rows(self, q, k, v, is_fp16: bool, causal: bool, scale: float,
+    def rows(self, q, k, v, is_fp16: bool, causal: int, scale: float,
              rows: np.ndarray, nthreads: int = 0) -> Tuple[np.ndarray, np.ndarray]:
         """Evaluate the query rows listed in ``rows`` (an n x 3 array of (b, h, i)).
+
+        causal: 0 none, 1 top-left (j <= i), 2 bottom-right (j <= i + Sk - Sq); True means 1.
 
         q is [B, Hq, Sq, D], k and v are [B, Hkv, Sk, D]: 16-bit patterns (numpy uint16)
         or torch bf16/fp16 tensors.  Returns (o [n, D] float64, lse [n] float64).
@@ -93,13 +97,13 @@ class Oracle:
         lse = np.empty((n,), dtype=np.float64)
         st = self.lib.fa_oracle_rows(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
                                      int(bool(is_fp16)), B, Hq, Hkv, Sq, Sk, D,
-                                     int(bool(causal)), float(scale), r.ctypes.data, n,
+                                     int(causal), float(scale), r.ctypes.data, n,
                                      o.ctypes.data, lse.ctypes.data, int(nthreads))
         if st != 0:
             raise ValueError(f"oracle rejected its arguments (status {st})")
         return o, lse
 
-    def full(self, q, k, v, is_fp16: bool, causal: bool, scale: float,
+    def full(self, q, k, v, is_fp16: bool, causal: int, scale: float,
              nthreads: int = 0) -> Tuple[np.ndarray, np.ndarray]:
         """Every query row: returns (o [B, Hq, Sq, D], lse [B, Hq, Sq]) in float64."""
         qb = _bits(q)

@@ -14,8 +14,12 @@
  *     definition instead of the recurrence;
  *   - "Como Domar o Blackwell Sem Enlouquecer com CUDA" (the FlashAttention-4 paragraph):
  *     grouped-query attention -- query head h reads key/value head h / (Hq / Hkv);
- *   - causal masking (named in the FAQ of the first page, no alignment given): key j is
- *     allowed for query row i when j <= i (top-left alignment);
+ *   - causal masking (named in the FAQ of the first page, no alignment given): with
+ *     causal == 1 key j is allowed for query row i when j <= i (top-left alignment); with
+ *     causal == 2 when j <= i + (Sk - Sq) (bottom-right alignment: the last query row sees
+ *     every key, as when new queries are appended after a cache of Sk - Sq keys);
+ *   - a row with no allowed key (possible only for causal == 2 with Sq > Sk) has an empty
+ *     softmax: its output is the empty sum, o = 0, and lse = ln 0 = -inf;
  *   - log-sum-exp of the scaled logits, natural log: lse = m + ln(sum_j exp(s_j - m)).
  *
  * Inputs are the raw 16-bit patterns of bf16 or fp16 tensors in [B, H, S, D] contiguous
@@ -91,15 +95,20 @@ static void attend_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     const int64_t qbase = ((b * Hq + h) * Sq + i) * D;
     const int64_t kvbase = (b * Hkv + kvh) * Sk * D;
 
-    /* allowed keys: j < Sk, and j <= i when causal */
+    /* allowed keys: j < Sk, and j <= i (causal 1) or j <= i + Sk - Sq (causal 2) */
     int64_t n_allowed = Sk;
+    if (causal) {
+        int64_t last = (causal == 2) ? i + (Sk - Sq) : i;   /* last allowed key index */
 #if FA_ORACLE_PLANT == 2
-    if (causal && i < Sk) n_allowed = i;         /* planted: causal bound off by one */
-#else
-    if (causal && i + 1 < Sk) n_allowed = i + 1;
+        last -= 1;                                        /* planted: causal bound off by one */
+#elif FA_ORACLE_PLANT == 8
+        if (causal == 2) last = i - (Sk - Sq);            /* planted: bottom-right offset sign */
 #endif
-    if (n_allowed <= 0) {
-        for (int64_t d = 0; d < D; ++d) o_row[d] = NAN;
+        if (last + 1 < n_allowed) n_allowed = last + 1;
+        if (n_allowed < 0) n_allowed = 0;
+    }
+    if (n_allowed == 0) {
+        for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;
         *lse_row = -INFINITY;
         return;
     }
@@ -168,7 +177,7 @@ int fa_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int 
                    int causal, double scale, const int64_t *rows, int64_t n_rows,
                    double *o_out, double *lse_out, int nthreads)
 {
-    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Sq < 0 || Sk < 0 || D < 1)
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Sq < 0 || Sk < 0 || D < 1 || causal < 0 || causal > 2)
         return -1;
     for (int64_t r = 0; r < n_rows; ++r) {
         const int64_t *t = rows + 3 * r;

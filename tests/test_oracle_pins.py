@@ -8,8 +8,9 @@ stray log-sum-exp term) to show that every such mistake fails at least one pin.
 
 What pins what:
   - torch's scaled_dot_product_attention in float64 on CPU (an independent library
-    routine the oracle never calls) for O, including GQA (enable_gqa) and causal
-    (is_causal, top-left aligned), on shapes with Sq != Sk, odd D and tiny heads;
+    routine the oracle never calls) for O, including GQA (enable_gqa), top-left causal
+    (is_causal) and bottom-right causal (an explicit lower-right boolean mask), on shapes
+    with Sq != Sk, odd D and tiny heads; rows left without keys are checked to be 0 / -inf;
   - torch.logsumexp over the masked score matrix for the log-sum-exp;
   - numpy's and torch's own bf16/fp16 decoders for every 16-bit pattern;
   - closed forms: scale = 0 (uniform weights), all keys equal, one key, two keys
@@ -49,12 +50,21 @@ SHAPES = [
 ]
 
 
+def _allowed(Sq, Sk, causal):
+    """Boolean [Sq, Sk] mask of allowed keys (built from torch.tril, not from the oracle)."""
+    ones = torch.ones(Sq, Sk, dtype=torch.bool)
+    if causal == 0:
+        return ones
+    return ones.tril(0 if causal == 1 else Sk - Sq)
+
+
 def pin_sdpa(orc):
-    """O against torch SDPA (float64, CPU), LSE against torch.logsumexp."""
+    """O against torch SDPA (float64, CPU), LSE against torch.logsumexp, for no mask,
+    top-left causal (SDPA's own is_causal) and bottom-right causal (explicit mask)."""
     seed = 10
     for (B, Hq, Hkv, Sq, Sk, D) in SHAPES:
         for dtype in (torch.bfloat16, torch.float16):
-            for causal in (False, True):
+            for causal in (0, 1, 2):
                 seed += 1
                 q = _rand_bits((B, Hq, Sq, D), dtype, seed)
                 k = _rand_bits((B, Hkv, Sk, D), dtype, seed + 1000)
@@ -62,14 +72,19 @@ def pin_sdpa(orc):
                 scale = 0.37 if D > 1 else 1.3
                 o, lse = orc.full(q, k, v, dtype == torch.float16, causal, scale)
                 qd, kd, vd = q.double(), k.double(), v.double()
-                ref = F.scaled_dot_product_attention(qd, kd, vd, is_causal=causal,
-                                                     scale=scale, enable_gqa=True)
-                np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+                mask = _allowed(Sq, Sk, causal)
+                if causal == 2:
+                    ref = F.scaled_dot_product_attention(qd, kd, vd, attn_mask=mask,
+                                                         scale=scale, enable_gqa=True)
+                else:
+                    ref = F.scaled_dot_product_attention(qd, kd, vd, is_causal=causal == 1,
+                                                         scale=scale, enable_gqa=True)
+                live = mask.any(dim=1).numpy()            # rows with at least one key
+                np.testing.assert_allclose(o[:, :, live], ref.numpy()[:, :, live], rtol=0, atol=1e-12)
+                assert np.all(o[:, :, ~live] == 0.0)      # empty softmax: o = 0
                 kx = kd.repeat_interleave(Hq // Hkv, dim=1)
                 s = scale * torch.einsum("bhid,bhjd->bhij", qd, kx)
-                if causal:
-                    mask = torch.ones(Sq, Sk, dtype=torch.bool).tril(0)
-                    s = s.masked_fill(~mask, float("-inf"))
+                s = s.masked_fill(~mask, float("-inf"))
                 np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(),
                                            rtol=0, atol=1e-12)
 
@@ -152,19 +167,24 @@ def pin_causal_future(orc):
 
 
 def pin_scale_zero(orc):
-    """scale = 0 -> uniform weights: o_i = mean of the allowed v_j, lse_i = ln |J_i|."""
-    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 10, 7, 3
-    q = _rand_bits((B, Hq, Sq, D), torch.float16, 13)
-    k = _rand_bits((B, Hkv, Sk, D), torch.float16, 14)
-    v = _rand_bits((B, Hkv, Sk, D), torch.float16, 15)
-    vd = v.double().numpy()
-    for causal in (False, True):
-        o, lse = orc.full(q, k, v, True, causal, 0.0)
-        for h in range(Hq):
-            for i in range(Sq):
-                n = min(i + 1, Sk) if causal else Sk
-                np.testing.assert_allclose(o[0, h, i], vd[0, h // 2, :n].mean(axis=0), rtol=0, atol=1e-14)
-                assert abs(lse[0, h, i] - math.log(n)) < 1e-14
+    """scale = 0 -> uniform weights: o_i = mean of the allowed v_j, lse_i = ln |J_i|, where
+    |J_i| = Sk, min(i+1, Sk) (top-left) or clamp(i+1+Sk-Sq, 0, Sk) (bottom-right)."""
+    B, Hq, Hkv, D = 1, 4, 2, 3
+    for (Sq, Sk) in ((10, 7), (4, 9)):
+        q = _rand_bits((B, Hq, Sq, D), torch.float16, 13)
+        k = _rand_bits((B, Hkv, Sk, D), torch.float16, 14)
+        v = _rand_bits((B, Hkv, Sk, D), torch.float16, 15)
+        vd = v.double().numpy()
+        for causal in (0, 1, 2):
+            o, lse = orc.full(q, k, v, True, causal, 0.0)
+            for h in range(Hq):
+                for i in range(Sq):
+                    n = (Sk, min(i + 1, Sk), max(0, min(i + 1 + Sk - Sq, Sk)))[causal]
+                    if n == 0:
+                        assert np.all(o[0, h, i] == 0.0) and lse[0, h, i] == -math.inf
+                        continue
+                    np.testing.assert_allclose(o[0, h, i], vd[0, h // 2, :n].mean(axis=0), rtol=0, atol=1e-14)
+                    assert abs(lse[0, h, i] - math.log(n)) < 1e-14
 
 
 def pin_equal_keys(orc):
@@ -201,6 +221,23 @@ def pin_two_keys_logistic(orc):
         assert abs(lse[0, 0, i] - logsumexp(s)) < 1e-13
 
 
+def pin_bottom_right_future(orc):
+    """Bottom-right causal: row i does not move when keys/values j > i + Sk - Sq change."""
+    B, H, Sq, Sk, D = 1, 2, 5, 9, 4
+    q = _rand_bits((B, H, Sq, D), torch.bfloat16, 30)
+    k = _rand_bits((B, H, Sk, D), torch.bfloat16, 31)
+    v = _rand_bits((B, H, Sk, D), torch.bfloat16, 32)
+    o1, l1 = orc.full(q, k, v, False, 2, 0.6)
+    for i in range(Sq):
+        last = i + Sk - Sq
+        k2, v2 = k.clone(), v.clone()
+        k2[:, :, last + 1:] = _rand_bits(k2[:, :, last + 1:].shape, torch.bfloat16, 300 + i)
+        v2[:, :, last + 1:] = _rand_bits(v2[:, :, last + 1:].shape, torch.bfloat16, 400 + i)
+        o2, l2 = orc.full(q, k2, v2, False, 2, 0.6)
+        np.testing.assert_array_equal(o1[:, :, i], o2[:, :, i])
+        np.testing.assert_array_equal(l1[:, :, i], l2[:, :, i])
+
+
 def pin_huge_logits(orc):
     """Logits far beyond exp's range stay finite: the largest one takes all the weight."""
     B, H, S, D = 1, 1, 4, 8
@@ -215,8 +252,8 @@ def pin_huge_logits(orc):
 
 
 PINS = [pin_sdpa, pin_decoders, pin_identical_value_rows, pin_single_key, pin_permutation,
-        pin_causal_future, pin_scale_zero, pin_equal_keys, pin_two_keys_logistic,
-        pin_huge_logits]
+        pin_causal_future, pin_bottom_right_future, pin_scale_zero, pin_equal_keys,
+        pin_two_keys_logistic, pin_huge_logits]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -226,7 +263,8 @@ def test_pin(orc, pin):
 
 PLANTS = {1: "wrong GQA head mapping", 2: "causal bound off by one",
           3: "transposed key operand", 4: "scale dropped", 5: "reversed value rows",
-          6: "normalised by key count", 7: "stray log-sum-exp term"}
+          6: "normalised by key count", 7: "stray log-sum-exp term",
+          8: "bottom-right offset with the wrong sign"}
 
 
 @pytest.mark.parametrize("plant", sorted(PLANTS), ids=[PLANTS[p] for p in sorted(PLANTS)])
