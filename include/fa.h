@@ -8,12 +8,16 @@
  *
  *   for every batch b, query head h and query row i:
  *     kvh       = h / (Hq / Hkv)                      (consecutive query heads share a KV head)
- *     J         = { j < Sk : causal == 0  or  j <= i } (top-left causal alignment)
+ *     J         = { j < Sk : causal == 0,  or j <= i (causal == 1, top-left),
+ *                   or j <= i + Sk - Sq (causal == 2, bottom-right) }
  *     s_j       = scale * sum_d q[b,h,i,d] * k[b,kvh,j,d]
  *     o[b,h,i,:]= sum_{j in J} exp(s_j - m) v[b,kvh,j,:] / sum_{j in J} exp(s_j - m),  m = max s_j
  *     lse[b,h,i]= m + ln sum_{j in J} exp(s_j - m)    (natural log, float32)
  *
  * computed tile by tile with an online softmax; the Sq x Sk score matrix is never stored.
+ * A row with no allowed key (only possible with causal == 2 and Sq > Sk) gets the empty-sum
+ * result: o = 0 and lse = -inf.  The pages name causal masking without an alignment; the
+ * bottom-right form serves queries appended after Sk - Sq cached keys.
  *
  * Layout (all tensors dense, row-major, no strides in the ABI):
  *   q   [B, Hq,  Sq, D]  16-bit (bf16 for fa_fwd, fp16 for fa_fwd_fp16)
@@ -59,13 +63,15 @@ typedef enum {
     FA_ERR_ARCH = 9,            /* current device is not compute capability 10.3 (sm_103)    */
     FA_ERR_TENSORMAP = 10,      /* cuTensorMapEncodeTiled unavailable or rejected the layout */
     FA_ERR_LAUNCH = 11,         /* the kernel launch failed (cudaGetLastError)               */
-    FA_ERR_DEVICE_TIMEOUT = 12  /* (fa_device_status) a bounded device-side wait expired     */
+    FA_ERR_DEVICE_TIMEOUT = 12, /* (fa_device_status) a bounded device-side wait expired     */
+    FA_ERR_CAUSAL = 13          /* causal not in {0, 1, 2}                                   */
 } fa_status_t;
 
 /*
  * fa_fwd -- bf16 attention forward.  Writes o and lse as described above.
  *   B, Hq, Hkv, Sq, Sk, D : sizes (D in {64, 128}; Hq % Hkv == 0)
- *   causal                : 0 = full attention, nonzero = key j allowed only for j <= i
+ *   causal                : 0 = full attention, 1 = key j allowed iff j <= i (top-left),
+ *                           2 = key j allowed iff j <= i + Sk - Sq (bottom-right)
  *   scale                 : multiplies q.k before the softmax (usually 1/sqrt(D))
  *   stream                : CUDA stream to enqueue on
  * B == 0 or Sq == 0 is a valid empty problem and returns FA_OK without touching memory.

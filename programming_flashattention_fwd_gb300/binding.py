@@ -22,7 +22,7 @@ STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_BAD_DIM", 3: "FA_ERR_HEADS",
     4: "FA_ERR_UNSUPPORTED_D", 5: "FA_ERR_ALIGN", 6: "FA_ERR_ALIAS", 7: "FA_ERR_SCALE",
     8: "FA_ERR_NO_DEVICE", 9: "FA_ERR_ARCH", 10: "FA_ERR_TENSORMAP", 11: "FA_ERR_LAUNCH",
-    12: "FA_ERR_DEVICE_TIMEOUT",
+    12: "FA_ERR_DEVICE_TIMEOUT", 13: "FA_ERR_CAUSAL",
 }
 
 _lib = None
@@ -97,13 +97,22 @@ def _check_tensors(q, k, v, o, lse):
         raise ValueError("q, k, v, o share one 16-bit dtype; lse is float32")
 
 
+def _causal_code(causal) -> int:
+    """False/0: none; True/1: top-left (j <= i); 2 or "bottom_right": j <= i + Sk - Sq."""
+    if causal in ("bottom_right", "bottom-right"):
+        return 2
+    if causal in ("top_left", "top-left"):
+        return 1
+    return int(causal)
+
+
 def _call(fn_name: str, q, k, v, o, lse, causal: bool, scale: float, stream, extra=()):
     _check_tensors(q, k, v, o, lse)
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     lib = load_library()
     st = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+                               B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale),
                                _stream_handle(stream), *extra)
     if st != 0:
         raise FaError(st, fa_strerror(st))

@@ -65,6 +65,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_HEADS;
     if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
+    if (causal < 0 || causal > 2) return FA_ERR_CAUSAL;
     if (B == 0 || Sq == 0) return FA_OK;
     if (Sk == 0) return FA_ERR_BAD_DIM;
     const long long BHq = (long long)B * Hq, BHkv = (long long)B * Hkv;
@@ -122,6 +123,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     // scale replaces every score by 0 (uniform weights), both exactly.
     p.smode = scale > 0.f ? 0u : (scale < 0.f ? 1u : 2u);
     p.sl2 = scale == 0.f ? 1.0f : (float)(std::fabs((double)scale) * 1.4426950408889634);
+    p.coff = causal == 2 ? Sk - Sq : 0;
     p.timeout_ns = timeout_ns;
     p.inject = inject;
 
@@ -168,6 +170,7 @@ const char *fa_strerror(int status)
     case FA_ERR_TENSORMAP: return "FA_ERR_TENSORMAP: TMA descriptor encoding failed";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a bounded device-side wait expired";
+    case FA_ERR_CAUSAL: return "FA_ERR_CAUSAL: causal must be 0 (none), 1 (top-left) or 2 (bottom-right)";
     default: return "unknown fa status code";
     }
 }

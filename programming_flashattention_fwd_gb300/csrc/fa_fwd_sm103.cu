@@ -127,8 +127,15 @@ __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
     u.tA = 2 * pr;
     u.tB = 2 * pr + 1;
     u.hasB = u.tB < p.Tq;
-    u.nA = CAUSAL ? min(p.Tk, u.tA + 1) : p.Tk;
-    u.nB = u.hasB ? (CAUSAL ? min(p.Tk, u.tB + 1) : p.Tk) : 0;
+    // key tiles a query tile needs: causal -> up to the tile holding key (last row + coff);
+    // 0 when even its last row has no allowed key (bottom-right alignment with Sq > Sk)
+    auto key_tiles = [&](int t) {
+        if (!CAUSAL) return p.Tk;
+        const long long hi = (long long)t * kBM + (kBM - 1) + p.coff;
+        return hi < 0 ? 0 : (int)min((long long)p.Tk, hi / kBN + 1);
+    };
+    u.nA = key_tiles(u.tA);
+    u.nB = u.hasB ? key_tiles(u.tB) : 0;
     u.n = max(u.nA, u.nB);
     return true;
 }
@@ -230,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             Unit u;
             for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
-                for (int x = 0; x < (u.hasB ? 2 : 1); ++x) {
+                for (int x = 0; x < 2; ++x) {
+                    if ((x ? u.nB : u.nA) == 0) continue;   // absent, or no allowed key at all
                     const int buf = tau % C::NQ;
                     if (tau >= C::NQ &&
                         !wait_bar(bar_qfree(buf), ((tau / C::NQ) - 1) & 1, abort_flag, tmo, SITE_QFREE)) {
@@ -289,17 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             Unit u;
             for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
-                const int nt = u.hasB ? 2 : 1;
-                const int buf[2] = {tau % C::NQ, (tau + 1) % C::NQ};
-                for (int x = 0; x < nt && ok; ++x)
-                    ok = wait_u(bar_q(buf[x]), ((tau + x) / C::NQ) & 1, SITE_MMA_Q);
-                tau += nt;
+                const int nt = 2;                      // tile slots; a slot with nk == 0 has no work
                 const int nk[2] = {u.nA, u.nB};
+                int buf[2] = {0, 0}, na = 0;
+                for (int x = 0; x < 2; ++x) {
+                    if (nk[x] == 0) continue;
+                    buf[x] = (tau + na) % C::NQ;
+                    ok = ok && wait_u(bar_q(buf[x]), ((tau + na) / C::NQ) & 1, SITE_MMA_Q);
+                    ++na;
+                }
+                tau += na;
+                if (na == 0) continue;                 // no query row of this unit has a key
                 const int uK0 = use;
                 if (ok) ok = wait_u(bar_full(uK0 % C::NS), (uK0 / C::NS) & 1, SITE_MMA_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 for (int x = 0; x < nt; ++x) {
+                    if (nk[x] == 0) continue;
                     issue_s(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE);
                     tc_commit_elect(barS0 + 8u * x);
                     if (nk[x] == 1) tc_commit_elect(bar_qfree(buf[x]));
@@ -366,6 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = x ? u.tB : u.tA;
             const int nk = x ? u.nB : u.nA;
             const int row = t * kBM + r;
+            if (nk == 0) {
+                // no allowed key for any row of this tile: the empty softmax, o = 0, lse = -inf
+                if (row < p.Sq) {
+                    uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)u.zq * p.Sq + row) * (size_t)(D * 2);
+#pragma unroll
+                    for (int c = 0; c < D * 2; c += 16) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
+                    p.lse[(size_t)u.zq * p.Sq + row] = -INFINITY;
+                }
+                continue;
+            }
 
             float m_used = -INFINITY;  // running max in exp2 units (possibly stale by <= kTau)
             float l = 0.f;             // running sum of p at m_used
@@ -404,25 +428,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal).
                 const int kbase = j * kBN;
                 const bool tail = kbase + kBN > p.Sk;
-                const bool diag = CAUSAL && (kbase + kBN - 1 > t * kBM);
+                const bool diag = CAUSAL && (kbase + kBN - 1 > t * kBM + p.coff);
                 if (tail || diag) {
                     int lim = p.Sk - 1 - kbase;
-                    if (CAUSAL) lim = min(lim, row - kbase);
+                    if (CAUSAL) lim = min(lim, row + p.coff - kbase);
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (c > lim) s[c] = -INFINITY;
                 }
 
-                float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-                float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+                // Row maximum: eight independent chains; 16 scores seed them, then each round of
+                // three-input max consumes 16 more (16 + 7 * 16 == 128 == kBN).
+                static_assert(kBN % 16 == 0 && kBN >= 16, "row-max chains cover the tile exactly");
+                float mx[8];
 #pragma unroll
-                for (int c = 12; c < kBN; c += 8) {
-                    mx0 = fmax3(mx0, s[c], s[c + 1]);
-                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                for (int c = 16; c + 16 <= kBN; c += 16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
                 }
-                const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                const float mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+                const float m_new = fmaxf(m_used, mrow * sl2);
 
                 float alpha = 1.f;
                 bool rescale = false;

@@ -22,6 +22,7 @@ struct Params {
     int num_units;      // work units (query-tile pairs) in the whole problem: B * Hq * NP
     float sl2;          // |scale| * log2(e): the exp2-domain multiplier of the scores
     uint32_t smode;     // 0: scale > 0; 1: scale < 0 (scores negated); 2: scale == 0 (scores zeroed)
+    int coff;           // causal offset: key j allowed for query i iff j <= i + coff (0 top-left, Sk - Sq bottom-right)
     uint64_t timeout_ns;// watchdog limit of each bounded wait
     uint32_t inject;    // fault-injection mask (0 in normal use)
 };

@@ -39,7 +39,7 @@ class Workload:
     Sk: int
     D: int
     dtype: str          # "bf16" or "fp16"
-    causal: bool
+    causal: int         # 0 none, 1 top-left (j <= i), 2 bottom-right (j <= i + Sk - Sq)
     seed: int
     q_std: float = 1.0
     k_std: float = 1.0
@@ -59,7 +59,8 @@ class Workload:
         return self.dtype == "fp16"
 
     def flops(self) -> float:
-        """Attention forward FLOPs: 4*B*Hq*Sq*Sk*D, halved when causal."""
+        """Attention forward FLOPs: 4*B*Hq*Sq*Sk*D, halved when causal (the benchmark's
+        convention for the square causal workloads)."""
         f = 4.0 * self.B * self.Hq * self.Sq * self.Sk * self.D
         return f / 2.0 if self.causal else f
 

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_function(lib):
 
 def test_strerror_covers_every_code(lib):
     codes = declared_status_codes()
-    assert len(codes) == 13 and sorted(codes.values()) == list(range(13))
+    assert len(codes) == 14 and sorted(codes.values()) == list(range(14))
     msgs = set()
     for name, val in codes.items():
         msg = lib.fa_strerror(val).decode()
@@ -74,6 +74,7 @@ def call(lib, fn="fa_fwd", q=Q, k=K, v=V, o=O, lse=L, **over):
     (dict(D=32), 4), (dict(D=96), 4), (dict(D=256), 4),
     (dict(scale=math.nan), 7), (dict(scale=math.inf), 7),
     (dict(B=100000, Hq=100000, Hkv=1), 2),
+    (dict(causal=3), 13), (dict(causal=-1), 13),
 ])
 def test_invalid_arguments(lib, fn, over, code):
     assert call(lib, fn, **over) == code

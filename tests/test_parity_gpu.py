@@ -9,7 +9,9 @@ same (rounded) inputs.
     tiles, the ragged last tile, first/last head and batch); every output row is checked
     to have been written (outputs are NaN-poisoned before the call);
   - a sweep of small shapes checked on every row: sequence lengths 1..513 (ragged tails,
-    single rows, single keys), Sq != Sk, GQA groups 1..8, D 64/128, bf16/fp16, causal on/off;
+    single rows, single keys), Sq != Sk, GQA groups 1..8, D 64/128, bf16/fp16, no mask /
+    top-left causal / bottom-right causal (including query tiles with no allowed key at all);
+  - a prefill-onto-cache shape (1000 new queries after 3096 cached keys, bottom-right);
   - guard canaries around every output buffer (no write outside o and lse);
   - bitwise determinism and a non-default stream;
   - the watchdog: an injected missing load makes the kernel give up, report
@@ -59,9 +61,11 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     og = o_gpu.detach().double().cpu().numpy() if isinstance(o_gpu, torch.Tensor) else o_gpu
     lg = lse_gpu.detach().double().cpu().numpy() if isinstance(lse_gpu, torch.Tensor) else lse_gpu
     assert np.all(np.isfinite(og)), f"{what}: non-finite O"
-    assert np.all(np.isfinite(lg)), f"{what}: non-finite lse"
+    empty = np.isneginf(lse_ref)                  # rows without an allowed key: o = 0, lse = -inf
+    assert np.all(np.isneginf(lg[empty])), f"{what}: empty rows need lse = -inf"
+    assert np.all(np.isfinite(lg[~empty])), f"{what}: non-finite lse"
     err = np.abs(og - o_ref)
-    lerr = np.abs(lg - lse_ref)
+    lerr = np.abs(lg[~empty] - lse_ref[~empty]) if (~empty).any() else np.zeros(1)
     assert err.max() <= MAX_ABS, f"{what}: max |dO| = {err.max():.3e}"
     assert err.mean() <= MEAN_ABS, f"{what}: mean |dO| = {err.mean():.3e}"
     assert lerr.max() <= LSE_ABS, f"{what}: max |dlse| = {lerr.max():.3e}"
@@ -86,8 +90,9 @@ for D in (64, 128):
     for (B, Hq, Hkv, Sq, Sk) in [(1, 1, 1, 1, 1), (1, 2, 1, 17, 17), (2, 4, 2, 127, 127),
                                  (1, 2, 2, 128, 128), (1, 3, 3, 129, 129), (1, 8, 1, 255, 255),
                                  (1, 2, 2, 256, 256), (1, 4, 2, 384, 200), (1, 2, 1, 200, 384),
-                                 (1, 2, 2, 513, 513), (2, 2, 2, 1, 300), (1, 2, 2, 300, 1)]:
-        for causal in (False, True):
+                                 (1, 2, 2, 513, 513), (2, 2, 2, 1, 300), (1, 2, 2, 300, 1),
+                                 (1, 2, 1, 513, 100), (1, 4, 2, 100, 513)]:
+        for causal in (0, 1, 2):
             SWEEP.append((B, Hq, Hkv, Sq, Sk, D, causal))
 
 
@@ -101,6 +106,32 @@ def test_shape_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
     o, lse = run_gpu(fa, w, q, k, v)
     o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
     check(o, lse, o_ref, l_ref, f"{w}")
+
+
+def test_bottom_right_prefill(fa, orc):
+    """1000 new query rows attending to 3096 cached keys plus themselves (bottom-right)."""
+    w = Workload("prefill", 1, 32, 8, 1000, 4096, 128, "bf16", 2, 21)
+    q, k, v = make_qkv(w)
+    o, lse = run_gpu(fa, w, q, k, v)
+    assert torch.isfinite(o).all().item() and torch.isfinite(lse).all().item()
+    rows = sample_rows(w, n=256)
+    o_ref, l_ref = orc.rows(q, k, v, False, 2, w.softmax_scale, rows)
+    r = torch.from_numpy(rows)
+    check(o.cpu()[r[:, 0], r[:, 1], r[:, 2]], lse.cpu()[r[:, 0], r[:, 1], r[:, 2]], o_ref, l_ref, "prefill")
+
+
+@pytest.mark.parametrize("seed", [5, 20031, 77, 123, 999])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_large_logit_rows(fa, orc, seed, causal):
+    """q, k with std 2 (logits ~ +-16): running maxima often jump by nearly 2^8 between
+    key tiles, where the lazy rescale keeps P near 256 and an inflated row maximum would
+    push P below the 16-bit range.  Checked on every row, fp16 and bf16."""
+    for dtype, D, Sq, Sk in (("fp16", 64, 200, 384), ("bf16", 128, 300, 700), ("fp16", 128, 513, 257)):
+        w = Workload("big", 1, 4, 2, Sq, Sk, D, dtype, causal, seed, q_std=2.0, k_std=2.0)
+        q, k, v = make_qkv(w)
+        o, lse = run_gpu(fa, w, q, k, v)
+        o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
+        check(o, lse, o_ref, l_ref, f"{w}")
 
 
 def test_scale_variants(fa, orc):
