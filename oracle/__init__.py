@@ -27,6 +27,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fa_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "ops_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 
 _handles = {}
@@ -43,11 +44,11 @@ def build(plant: int = 0, out_dir: Optional[str] = None) -> str:
     os.makedirs(out_dir, exist_ok=True)
     name = "libfa_oracle.so" if plant == 0 else f"libfa_oracle_plant{plant}.so"
     out = os.path.join(out_dir, name)
-    if plant == 0 and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+    if plant == 0 and os.path.exists(out) and all(os.path.getmtime(out) >= os.path.getmtime(x) for x in _SRCS):
         return out
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
-           f"-DFA_ORACLE_PLANT={int(plant)}", _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c99", "-D_DEFAULT_SOURCE", "-fPIC", "-shared", "-fopenmp",
+           f"-DFA_ORACLE_PLANT={int(plant)}", *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -70,6 +71,17 @@ class Oracle:
         d.restype = ctypes.c_double
         d.argtypes = [ctypes.c_uint16, ctypes.c_int]
         self.lib.fa_oracle_max_threads.restype = ctypes.c_int
+        g = self.lib.fa_oracle_gemm_entries
+        g.restype = ctypes.c_int
+        g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                      ctypes.c_void_p]
+        sm = self.lib.fa_oracle_softmax_rows
+        sm.restype = ctypes.c_int
+        sm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                       ctypes.c_int64, ctypes.c_void_p]
+        self.lib.fa_oracle_gelu_tanh.restype = ctypes.c_double
+        self.lib.fa_oracle_gelu_tanh.argtypes = [ctypes.c_double]
 
     def max_threads(self) -> int:
         return int(self.lib.fa_oracle_max_threads())
@@ -111,6 +123,76 @@ class Oracle:
         rows = all_rows(B, Hq, Sq)
         o, lse = self.rows(qb, k, v, is_fp16, causal, scale, rows, nthreads)
         return o.reshape(B, Hq, Sq, D), lse.reshape(B, Hq, Sq)
+
+
+    # ---------------------------------------------------------------- building blocks
+    def gemm_entries(self, a, b, is_fp16: bool, entries, bias=None, epilogue: int = 0) -> np.ndarray:
+        """epilogue(A @ B) at the listed (m, n) entries; A [M,K], B [K,N] 16-bit (bits or tensors).
+        epilogue: 0 none, 1 + bias[n], 2 tanh-GELU(. + bias[n]); bias is float32 [N]."""
+        ab, bb = _bits(a), _bits(b)
+        M, K = ab.shape
+        Kb, N = bb.shape
+        if Kb != K:
+            raise ValueError("inner dimensions differ")
+        e = np.ascontiguousarray(np.asarray(entries, dtype=np.int64).reshape(-1, 2))
+        out = np.empty(e.shape[0], dtype=np.float64)
+        bptr = None
+        if epilogue:
+            bias = np.ascontiguousarray(np.asarray(_as_numpy(bias), dtype=np.float32).reshape(-1))
+            if bias.shape[0] != N:
+                raise ValueError("bias must have N entries")
+            bptr = bias.ctypes.data
+        st = self.lib.fa_oracle_gemm_entries(ab.ctypes.data, bb.ctypes.data, int(bool(is_fp16)), M, N, K,
+                                             bptr, int(epilogue), e.ctypes.data, e.shape[0], out.ctypes.data)
+        if st != 0:
+            raise ValueError(f"oracle rejected its arguments (status {st})")
+        return out
+
+    def gemm_full(self, a, b, is_fp16: bool, bias=None, epilogue: int = 0) -> np.ndarray:
+        ab, bb = _bits(a), _bits(b)
+        M, N = ab.shape[0], bb.shape[1]
+        mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+        ent = np.stack([mm.ravel(), nn.ravel()], axis=1)
+        return self.gemm_entries(ab, bb, is_fp16, ent, bias, epilogue).reshape(M, N)
+
+    def softmax_rows(self, x, row_ids=None) -> np.ndarray:
+        """Row softmax of the listed rows of x [rows, cols] (fp32 array/tensor or bf16 tensor)."""
+        xf, xb = None, None
+        try:
+            import torch
+            if isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16:
+                xb = _bits(x)
+            elif isinstance(x, torch.Tensor):
+                xf = np.ascontiguousarray(x.detach().cpu().float().numpy())
+        except ImportError:
+            pass
+        if xf is None and xb is None:
+            xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+        arr = xf if xf is not None else xb
+        rows, cols = arr.shape
+        ids = np.arange(rows, dtype=np.int64) if row_ids is None else np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
+        out = np.empty((ids.shape[0], cols), dtype=np.float64)
+        st = self.lib.fa_oracle_softmax_rows(xf.ctypes.data if xf is not None else None,
+                                             xb.ctypes.data if xb is not None else None,
+                                             rows, cols, ids.ctypes.data, ids.shape[0], out.ctypes.data)
+        if st != 0:
+            raise ValueError(f"oracle rejected its arguments (status {st})")
+        return out
+
+    def gelu_tanh(self, h: float) -> float:
+        return float(self.lib.fa_oracle_gelu_tanh(float(h)))
+
+
+def _as_numpy(x):
+    if isinstance(x, np.ndarray):
+        return x
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().cpu().float().numpy()
+    except ImportError:
+        pass
+    return np.asarray(x)
 
 
 def all_rows(B: int, H: int, S: int) -> np.ndarray:
