@@ -18,6 +18,11 @@ query rows, on all host cores.
 ``--impl reference`` times that oracle instead (the reference arm: there is no other
 implementation of these pages to run): each step evaluates a bounded sample of query rows.
 
+``--op gemm | gemm_gelu | softmax`` measures the standalone building blocks instead of the
+attention call (same JSON fields): the tiled matrix product (bf16, M = N = K = 8192 by
+default; ``gemm_gelu`` adds the fused bias + tanh-GELU epilogue), against the tensor roofline,
+and the row softmax (fp32, 65536 x 4096 by default), against the HBM roofline.
+
 Multi-GPU (torchrun, one process per GPU): every rank runs its own replica of the workload
 (independent inputs, no collective on the data path); timings are max-reduced across ranks
 and ``value`` counts the work of all ranks (weak scaling).
@@ -41,6 +46,7 @@ sys.path.insert(0, ROOT)
 METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak (causal / non-causal)"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
 
@@ -65,6 +71,14 @@ def measured_peaks():
         return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
     except Exception:
         return FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+def measured_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
 
 
 def ncu_traffic(workload: str):
@@ -370,6 +384,149 @@ def run_ours(args, w, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_op(args, world, rank, local):
+    """Standalone building blocks: tiled matrix product (+ fused epilogue) or row softmax."""
+    import numpy as np
+    import torch
+    import oracle
+    from programming_flashattention_fwd_gb300 import binding
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    g = torch.Generator().manual_seed(1234 + 7919 * rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    if args.op in ("gemm", "gemm_gelu"):
+        M, N, K = args.M, args.N, args.K
+        epi = 2 if args.op == "gemm_gelu" else 0
+        a_h = torch.randn((M, K), generator=g).to(torch.bfloat16)
+        b_h = torch.randn((K, N), generator=g).to(torch.bfloat16)
+        bias_h = torch.randn((N,), generator=g)
+        a, b, bias = a_h.to(dev), b_h.to(dev), bias_h.to(dev)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        call = lambda: binding.gemm(a, b, bias if epi else None, epi, False, c)
+        work = 2.0 * M * N * K
+        name = f"{args.op}_bf16_{M}x{N}x{K}"
+        metric, unit, bound = ("matrix product TFLOP/s" + (" (bias + tanh-GELU epilogue)" if epi else ""),
+                               "TFLOP/s", "tensor")
+        scale = 1e12
+        cfg = {"workload": name, "M": M, "N": N, "K": K, "dtype": "bf16", "out": "bf16", "epilogue": epi}
+        h2d = (a_h.numel() + b_h.numel()) * 2 + (bias_h.numel() * 4 if epi else 0)
+        d2h = c.numel() * 2
+    else:
+        R, C = args.rows, args.cols
+        x_h = torch.randn((R, C), generator=g) * 4.0
+        x = x_h.to(dev)
+        y = torch.empty_like(x)
+        call = lambda: binding.softmax_rows(x, y)
+        work = 2.0 * R * C * 4
+        name = f"softmax_fp32_{R}x{C}"
+        metric, unit, bound = "row softmax GB/s (bytes read + written)", "GB/s", "hbm"
+        scale = 1e9
+        cfg = {"workload": name, "rows": R, "cols": C, "dtype": "fp32"}
+        h2d, d2h = x_h.numel() * 4, x_h.numel() * 4
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark("start")
+    for s_ in range(args.steps):
+        flush.zero_()
+        starts[s_].record(stream)
+        call()
+        ends[s_].record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark("end")
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    t_step = max_over_ranks(sum(a_.elapsed_time(b_) * 1e-3 for a_, b_ in zip(starts, ends)) / args.steps, world)
+    st, word = binding.fa_device_status()
+    if st != 0:
+        raise RuntimeError(f"device watchdog fired (word {word:#x})")
+
+    # end to end: pinned host inputs in, result out, inside the events
+    if args.op in ("gemm", "gemm_gelu"):
+        a_p, b_p, bias_p = a_h.pin_memory(), b_h.pin_memory(), bias_h.pin_memory()
+        c_p = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+        def e2e():
+            a.copy_(a_p, non_blocking=True)
+            b.copy_(b_p, non_blocking=True)
+            if epi:
+                bias.copy_(bias_p, non_blocking=True)
+            call()
+            c_p.copy_(c, non_blocking=True)
+    else:
+        x_p = x_h.pin_memory()
+        y_p = torch.empty_like(x_h).pin_memory()
+
+        def e2e():
+            x.copy_(x_p, non_blocking=True)
+            call()
+            y_p.copy_(y, non_blocking=True)
+    for _ in range(max(1, args.warmup)):
+        e2e()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, world)
+    if rank != 0:
+        return
+
+    if bound == "tensor":
+        peak, _, src = measured_peaks()
+        peak_unit = "TFLOP/s"
+    else:
+        peak, src = measured_hbm()
+        peak_unit = "GB/s"
+    achieved = work / t_step / scale
+    orc = oracle.load()
+    t0 = time.perf_counter()
+    if args.op in ("gemm", "gemm_gelu"):
+        rng = np.random.default_rng(5)
+        n_ent = max(64, int(4e8 / K / 8))   # sized for a few seconds of float64 work on the host
+        ent = np.stack([rng.integers(0, M, n_ent), rng.integers(0, N, n_ent)], 1)
+        orc.gemm_entries(a_h, b_h, False, ent, bias_h if epi else None, epi)
+        cpu_work, sample = 2.0 * K * n_ent, f"{n_ent} seeded output entries of {name}, float64 C oracle"
+    else:
+        ids = np.random.default_rng(5).integers(0, R, 512)
+        orc.softmax_rows(x_h, ids)
+        cpu_work, sample = 2.0 * len(ids) * C * 4, f"{len(ids)} seeded rows of {name}, float64 C oracle"
+    dt = time.perf_counter() - t0
+    line = {
+        "metric": metric, "value": work * world / t_step / scale, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic",
+        "config": dict(cfg, l2="flushed between timed steps (256 MiB write)",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "e2e": {"value": work * world / t_e2e / scale, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": peak_unit,
+                     "frac": achieved / peak, "traffic": ncu_traffic(name),
+                     "peak_source": f"{src}" + (" dense bf16 (burst)" if bound == "tensor" else " HBM copy"),
+                     "kernel": "fa::gemm::gemm_kernel" if bound == "tensor" else "fa::sm::softmax_regs_kernel"},
+        "clocks": clocks,
+        "cpu_baseline": {"value": cpu_work / dt / scale, "unit": unit, "cores": orc.max_threads(),
+                         "kind": "oracle", "sample": sample + f", {dt:.1f} s"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     from programming_flashattention_fwd_gb300.inputs import DEFAULT_BENCH_WORKLOAD, WORKLOADS
     ap = argparse.ArgumentParser()
@@ -382,6 +539,12 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=90.0, help="reference-arm total budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--op", default="attention", choices=["attention", "gemm", "gemm_gelu", "softmax"])
+    ap.add_argument("--M", type=int, default=8192)
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--K", type=int, default=8192)
+    ap.add_argument("--rows", type=int, default=65536)
+    ap.add_argument("--cols", type=int, default=4096)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -389,7 +552,13 @@ def main():
     world, rank, local = dist_init()
     if world != args.gpus and world > 1:
         args.gpus = world
-    if args.impl == "reference":
+    if args.op != "attention":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the attention call only"}))
+        else:
+            run_op(args, world, rank, local)
+    elif args.impl == "reference":
         run_reference(args, w, world, rank)
     else:
         run_ours(args, w, world, rank, local)

@@ -64,7 +64,9 @@ typedef enum {
     FA_ERR_TENSORMAP = 10,      /* cuTensorMapEncodeTiled unavailable or rejected the layout */
     FA_ERR_LAUNCH = 11,         /* the kernel launch failed (cudaGetLastError)               */
     FA_ERR_DEVICE_TIMEOUT = 12, /* (fa_device_status) a bounded device-side wait expired     */
-    FA_ERR_CAUSAL = 13          /* causal not in {0, 1, 2}                                   */
+    FA_ERR_CAUSAL = 13,         /* causal not in {0, 1, 2}                                   */
+    FA_ERR_SHAPE = 14,          /* (fa_gemm) K or N not a multiple of 8 (16-byte rows)       */
+    FA_ERR_ARG = 15             /* an enum-like argument (dtype, output type, epilogue) is out of range */
 } fa_status_t;
 
 /*
@@ -109,6 +111,34 @@ int fa_device_status(fa_stream_t stream, uint32_t *detail);
 int fa_fwd_debug(const void *q, const void *k, const void *v, void *o, float *lse,
                  int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                  fa_stream_t stream, int is_fp16, uint64_t timeout_ns, uint32_t inject);
+
+/*
+ * fa_gemm -- tiled matrix product with an optional fused epilogue, the tutorial's building
+ * block for both attention products ("Guia Prático de Programação de GPU com Tiles", section 5:
+ * K-loop tiling with an fp32 accumulator; section 3 and the course's lesson 9: bias and
+ * tanh-GELU fused into the same pass):
+ *     epilogue 0: C = A B
+ *     epilogue 1: C = A B + bias            (bias broadcast over rows)
+ *     epilogue 2: C = gelu_tanh(A B + bias), gelu_tanh(h) = 0.5 h (1 + tanh(sqrt(2/pi)(h + 0.044715 h^3)))
+ *   a     [M, K] row-major, b [K, N] row-major: bf16 (dtype 0) or fp16 (dtype 1), device pointers
+ *   c     [M, N] row-major: the input type (out_fp32 0, round to nearest even) or float32 (1)
+ *   bias  [N] float32 device pointer; required for epilogues 1 and 2, ignored for 0
+ * K and N must be multiples of 8 (16-byte rows for TMA); a, b, c 16-byte aligned.  M, N or K
+ * need not be tile multiples.  M == 0 or N == 0 is an empty no-op.  c must not overlap a, b
+ * or bias.  Asynchronous on `stream`; returns FA_OK or a status code (no CUDA call is made
+ * for invalid arguments).
+ */
+int fa_gemm(const void *a, const void *b, void *c, const float *bias, int M, int N, int K,
+            int dtype, int out_fp32, int epilogue, fa_stream_t stream);
+
+/*
+ * fa_softmax_rows -- numerically stable softmax of every row of x ("Guia Prático de
+ * Programação de GPU com Tiles", section 4): y[r, :] = exp(x[r, :] - max) / sum exp(x[r, :] - max).
+ *   x, y  [rows, cols] row-major device arrays, float32 (dtype 0) or bf16 (dtype 1)
+ * y may be x (in place) but may not partially overlap it.  rows == 0 is a no-op; cols must
+ * be >= 1.  Asynchronous on `stream`.
+ */
+int fa_softmax_rows(const void *x, void *y, int rows, int cols, int dtype, fa_stream_t stream);
 
 #ifdef __cplusplus
 }

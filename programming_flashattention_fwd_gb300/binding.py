@@ -22,7 +22,7 @@ STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_BAD_DIM", 3: "FA_ERR_HEADS",
     4: "FA_ERR_UNSUPPORTED_D", 5: "FA_ERR_ALIGN", 6: "FA_ERR_ALIAS", 7: "FA_ERR_SCALE",
     8: "FA_ERR_NO_DEVICE", 9: "FA_ERR_ARCH", 10: "FA_ERR_TENSORMAP", 11: "FA_ERR_LAUNCH",
-    12: "FA_ERR_DEVICE_TIMEOUT", 13: "FA_ERR_CAUSAL",
+    12: "FA_ERR_DEVICE_TIMEOUT", 13: "FA_ERR_CAUSAL", 14: "FA_ERR_SHAPE", 15: "FA_ERR_ARG",
 }
 
 _lib = None
@@ -48,6 +48,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.fa_strerror.argtypes = [ctypes.c_int]
     lib.fa_device_status.restype = ctypes.c_int
     lib.fa_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.fa_gemm.restype = ctypes.c_int
+    lib.fa_gemm.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    lib.fa_softmax_rows.restype = ctypes.c_int
+    lib.fa_softmax_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_void_p]
     return lib
 
 
@@ -158,3 +163,43 @@ def fa_device_status(stream=None) -> Tuple[int, int]:
     w = ctypes.c_uint32(0)
     st = load_library().fa_device_status(_stream_handle(stream), ctypes.byref(w))
     return int(st), int(w.value)
+
+
+def gemm(a, b, bias=None, epilogue: int = 0, out_fp32: bool = False, c=None, stream=None):
+    """C = epilogue(A @ B) on the GPU (fa_gemm): a [M,K], b [K,N] bf16/fp16 CUDA tensors,
+    bias [N] float32 for epilogue 1 (+bias) and 2 (tanh-GELU(. + bias)).  Returns c."""
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError("a must be [M, K] and b [K, N]")
+    if a.dtype != b.dtype or a.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("a and b share one 16-bit dtype")
+    for name, t in (("a", a), ("b", b)):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    M, K = a.shape
+    N = b.shape[1]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32 if out_fp32 else a.dtype, device=a.device)
+    if epilogue and (bias is None or bias.dtype != torch.float32 or bias.numel() != N or not bias.is_cuda):
+        raise ValueError("epilogues 1 and 2 need a float32 CUDA bias of N entries")
+    st = load_library().fa_gemm(a.data_ptr(), b.data_ptr(), c.data_ptr(), bias.data_ptr() if epilogue else None,
+                                M, N, K, 0 if a.dtype == torch.bfloat16 else 1, int(bool(out_fp32)), int(epilogue),
+                                _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, fa_strerror(st))
+    return c
+
+
+def softmax_rows(x, y=None, stream=None):
+    """Row softmax on the GPU (fa_softmax_rows): x [rows, cols] float32 or bf16 CUDA tensor;
+    y defaults to a new tensor (pass y=x for in place).  Returns y."""
+    if x.dim() != 2 or x.dtype not in (torch.float32, torch.bfloat16) or not (x.is_cuda and x.is_contiguous()):
+        raise ValueError("x must be a contiguous 2-D float32 or bf16 CUDA tensor")
+    if y is None:
+        y = torch.empty_like(x)
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous():
+        raise ValueError("y must match x")
+    st = load_library().fa_softmax_rows(x.data_ptr(), y.data_ptr(), x.shape[0], x.shape[1],
+                                        0 if x.dtype == torch.float32 else 1, _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, fa_strerror(st))
+    return y

@@ -131,9 +131,97 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// 2-D view (inner, outer) of a row-major 16-bit matrix; box inner x outer, 128B swizzle.
+bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, long long inner, long long outer,
+               int box_inner, int box_outer)
+{
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Device checks shared by every entry point (current device must be sm_103).
+int check_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
+    int st = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_NO_DEVICE;
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        g_arch_ok[dev].store(st, std::memory_order_relaxed);
+    }
+    return st == 1 ? FA_OK : FA_ERR_ARCH;
+}
+
 } // namespace
 
 extern "C" {
+
+int fa_gemm(const void *a, const void *b, void *c, const float *bias, int M, int N, int K, int dtype, int out_fp32,
+            int epilogue, fa_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return FA_ERR_BAD_DIM;
+    if ((dtype != 0 && dtype != 1) || (out_fp32 != 0 && out_fp32 != 1) || epilogue < 0 || epilogue > 2)
+        return FA_ERR_ARG;
+    if (M == 0 || N == 0) return FA_OK;
+    if (K == 0) return FA_ERR_BAD_DIM;
+    if (K % 8 != 0 || N % 8 != 0) return FA_ERR_SHAPE;
+    const long long Tm = (M + 127) / 128, Tn = (N + 255) / 256, nK = (K + 63) / 64;
+    if (Tm * Tn > 0x7fffffffLL) return FA_ERR_BAD_DIM;
+    if (!a || !b || !c || (epilogue && !bias)) return FA_ERR_NULL_PTR;
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16) || (bias && !aligned(bias, 4))) return FA_ERR_ALIGN;
+    const size_t na = (size_t)M * K * 2, nb = (size_t)K * N * 2, nc = (size_t)M * N * (out_fp32 ? 4 : 2);
+    if (ranges_overlap(c, nc, a, na) || ranges_overlap(c, nc, b, nb) ||
+        (bias && ranges_overlap(c, nc, bias, (size_t)N * 4)))
+        return FA_ERR_ALIAS;
+    int st = check_device();
+    if (st != FA_OK) return st;
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return FA_ERR_TENSORMAP;
+    const bool bf16 = dtype == 0;
+    CUtensorMap ma, mb;
+    if (!encode_2d(enc, &ma, a, bf16, K, M, 64, 128) || !encode_2d(enc, &mb, b, bf16, N, K, 64, 64))
+        return FA_ERR_TENSORMAP;
+    fa::GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.c = c;
+    p.bias = epilogue ? bias : nullptr;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.Tm = (int)Tm;
+    p.Tn = (int)Tn;
+    p.nK = (int)nK;
+    p.num_tiles = (int)(Tm * Tn);
+    cudaError_t e = fa::launch_gemm(bf16, out_fp32 != 0, epilogue, ma, mb, p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_softmax_rows(const void *x, void *y, int rows, int cols, int dtype, fa_stream_t stream)
+{
+    if (rows < 0 || cols < 0) return FA_ERR_BAD_DIM;
+    if (dtype != 0 && dtype != 1) return FA_ERR_ARG;
+    if (rows == 0) return FA_OK;
+    if (cols == 0) return FA_ERR_BAD_DIM;
+    if (!x || !y) return FA_ERR_NULL_PTR;
+    const uintptr_t al = dtype == 0 ? 4 : 2;
+    if (!aligned(x, al) || !aligned(y, al)) return FA_ERR_ALIGN;
+    const size_t n = (size_t)rows * cols * (dtype == 0 ? 4 : 2);
+    if (x != y && ranges_overlap(x, n, y, n)) return FA_ERR_ALIAS;   // in place is fine, partial overlap is not
+    int st = check_device();
+    if (st != FA_OK) return st;
+    cudaError_t e = fa::launch_softmax_rows(dtype == 1, x, y, rows, cols, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
            int D, int causal, float scale, fa_stream_t stream)
@@ -171,14 +259,18 @@ const char *fa_strerror(int status)
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a bounded device-side wait expired";
     case FA_ERR_CAUSAL: return "FA_ERR_CAUSAL: causal must be 0 (none), 1 (top-left) or 2 (bottom-right)";
+    case FA_ERR_SHAPE: return "FA_ERR_SHAPE: matrix rows must be 16-byte multiples (K and N multiples of 8)";
+    case FA_ERR_ARG: return "FA_ERR_ARG: dtype, output type or epilogue selector out of range";
     default: return "unknown fa status code";
     }
 }
 
 int fa_device_status(fa_stream_t stream, uint32_t *detail)
 {
-    uint32_t w = 0;
+    uint32_t w = 0, wg = 0;
     if (fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &w) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    if (fa::read_and_clear_gemm_status(&wg) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    if (!(w & 1u)) w = wg;   // first expiry wins; attention's word is checked first
     if (detail) *detail = w;
     return (w & 1u) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }

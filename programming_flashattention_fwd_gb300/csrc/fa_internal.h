@@ -38,4 +38,23 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const Maps &maps, const Pa
 // Reads and clears the current device's watchdog word (synchronous on `stream`).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word);
 
+// ---------------------------------------------------------------- tiled matrix product
+struct GemmParams {
+    void *c;               // [M, N] row-major, 16-bit (input type) or fp32
+    const float *bias;     // [N] fp32, or nullptr when the epilogue has no bias
+    int M, N, K;
+    int Tm, Tn, nK;        // 128-row tiles, 256-column tiles, 64-wide K blocks
+    int num_tiles;         // Tm * Tn
+    uint64_t timeout_ns;
+};
+// epilogue: 0 none, 1 + bias, 2 tanh-GELU(. + bias).  A map: 2-D (K, M), box 64 x 128;
+// B map: 2-D (N, K), box 64 x 64; both 128B swizzle.
+cudaError_t launch_gemm(bool bf16, bool out_f32, int epilogue, const CUtensorMap &a, const CUtensorMap &b,
+                        const GemmParams &p, cudaStream_t stream);
+cudaError_t read_and_clear_gemm_status(uint32_t *word);
+
+// ---------------------------------------------------------------- row softmax
+// x, y: [rows, cols] row-major, fp32 or bf16 (same type); one launch, any cols >= 1.
+cudaError_t launch_softmax_rows(bool bf16, const void *x, void *y, int rows, int cols, cudaStream_t stream);
+
 } // namespace fa

@@ -337,4 +337,21 @@ __host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo_bytes)
     return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
+// 2-D tiled load global -> shared; completion is signalled as tx bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+// Bytes of dynamic shared memory the running kernel was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_size_u32()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
 } // namespace fa

@@ -35,7 +35,8 @@ def declared_status_codes():
 
 def test_header_declares_the_entry_points():
     fns = declared_functions()
-    for name in ("fa_fwd", "fa_fwd_fp16", "fa_strerror", "fa_device_status", "fa_fwd_debug"):
+    for name in ("fa_fwd", "fa_fwd_fp16", "fa_strerror", "fa_device_status", "fa_fwd_debug", "fa_gemm",
+                 "fa_softmax_rows"):
         assert name in fns
 
 
@@ -46,7 +47,7 @@ def test_library_exports_every_declared_function(lib):
 
 def test_strerror_covers_every_code(lib):
     codes = declared_status_codes()
-    assert len(codes) == 14 and sorted(codes.values()) == list(range(14))
+    assert len(codes) == 16 and sorted(codes.values()) == list(range(16))
     msgs = set()
     for name, val in codes.items():
         msg = lib.fa_strerror(val).decode()
@@ -112,3 +113,40 @@ def test_debug_entry_point_validates_the_same_way(lib):
     f = lib.fa_fwd_debug
     assert f(Q, K, V, O, L, 1, 3, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0) == 3
     assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 80, 0, 1.0, None, 1, 0, 0) == 4
+
+
+# fa_gemm(a, b, c, bias, M, N, K, dtype, out_fp32, epilogue, stream) -- every call rejected before CUDA
+GG = dict(M=256, N=512, K=128, dtype=0, out=0, epi=2)
+A_, B_, C_, BIAS = 0x60000000, 0x70000000, 0x80000000, 0x90000000
+
+
+def gemm_call(lib, a=A_, b=B_, c=C_, bias=BIAS, **over):
+    g = dict(GG, **over)
+    return lib.fa_gemm(a, b, c, bias, g["M"], g["N"], g["K"], g["dtype"], g["out"], g["epi"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(M=-1), 2), (dict(K=-8), 2), (dict(K=0), 2),
+    (dict(dtype=2), 15), (dict(out=3), 15), (dict(epi=3), 15), (dict(epi=-1), 15),
+    (dict(K=12), 14), (dict(N=100), 14),
+    (dict(a=None), 1), (dict(c=None), 1), (dict(bias=None), 1),
+    (dict(a=A_ + 8), 5), (dict(c=C_ + 2), 5), (dict(bias=BIAS + 2), 5),
+    (dict(c=A_ + 64), 6), (dict(c=BIAS - 64, bias=BIAS), 6),
+])
+def test_gemm_invalid_arguments(lib, over, code):
+    assert gemm_call(lib, **over) == code
+
+
+def test_gemm_empty_and_bias_optional(lib):
+    assert gemm_call(lib, M=0) == 0 and gemm_call(lib, N=0, a=None, b=None, c=None) == 0
+    # no bias needed without an epilogue: rejected later only by the overlap check here
+    assert gemm_call(lib, epi=0, bias=None, c=A_ + 16) == 6
+
+
+@pytest.mark.parametrize("args,code", [
+    ((Q, O, -1, 8, 0), 2), ((Q, O, 4, 0, 0), 2), ((Q, O, 4, 8, 2), 15), ((None, O, 4, 8, 0), 1),
+    ((Q + 2, O, 4, 8, 0), 5), ((Q + 1, O, 4, 8, 1), 5), ((Q, Q + 8, 4, 8, 0), 6), ((Q, O, 0, 8, 0), 0),
+])
+def test_softmax_invalid_arguments(lib, args, code):
+    x, y, rows, cols, dtype = args
+    assert lib.fa_softmax_rows(x, y, rows, cols, dtype, None) == code
