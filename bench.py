@@ -496,7 +496,9 @@ def run_op(args, world, rank, local):
     achieved = work / t_step / scale
     orc = oracle.load()
     t0 = time.perf_counter()
-    if args.op in ("gemm", "gemm_gelu"):
+    if args.no_cpu_baseline:
+        cpu_work, sample = None, None
+    elif args.op in ("gemm", "gemm_gelu"):
         rng = np.random.default_rng(5)
         n_ent = max(64, int(4e8 / K / 8))   # sized for a few seconds of float64 work on the host
         ent = np.stack([rng.integers(0, M, n_ent), rng.integers(0, N, n_ent)], 1)
@@ -521,9 +523,10 @@ def run_op(args, world, rank, local):
                      "peak_source": f"{src}" + (" dense bf16 (burst)" if bound == "tensor" else " HBM copy"),
                      "kernel": "fa::gemm::gemm_kernel" if bound == "tensor" else "fa::sm::softmax_regs_kernel"},
         "clocks": clocks,
-        "cpu_baseline": {"value": cpu_work / dt / scale, "unit": unit, "cores": orc.max_threads(),
-                         "kind": "oracle", "sample": sample + f", {dt:.1f} s"},
     }
+    if cpu_work is not None:
+        line["cpu_baseline"] = {"value": cpu_work / dt / scale, "unit": unit, "cores": orc.max_threads(),
+                                "kind": "oracle", "sample": sample + f", {dt:.1f} s"}
     print(json.dumps(line), flush=True)
 
 
