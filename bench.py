@@ -269,7 +269,7 @@ def run_reference(args, w, world, rank):
 
 
 def workload_config(w, args):
-    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+    return {"workload": w.name, "kernel": getattr(args, "kernel", 0), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
             "dtype": w.dtype, "causal": w.causal, "scale": w.softmax_scale, "seed": w.seed,
             "l2": "flushed between timed steps (256 MiB write)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
@@ -290,7 +290,10 @@ def run_ours(args, w, world, rank, local):
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    fn = binding.fa_fwd_fp16 if w.is_fp16 else binding.fa_fwd
+    if args.kernel:
+        fn = lambda q_, k_, v_, o_, l_, c_, s_: binding.fa_fwd_select(q_, k_, v_, o_, l_, c_, s_, args.kernel)
+    else:
+        fn = binding.fa_fwd_fp16 if w.is_fp16 else binding.fa_fwd
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -531,7 +534,7 @@ def run_op(args, world, rank, local):
 
 
 def main():
-    from programming_flashattention_fwd_gb300.inputs import DEFAULT_BENCH_WORKLOAD, WORKLOADS
+    from programming_flashattention_fwd_gb300.inputs import ALL_WORKLOADS as WORKLOADS, DEFAULT_BENCH_WORKLOAD
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -542,6 +545,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=90.0, help="reference-arm total budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="attention kernel variant: 0 automatic, 1 two tiles / 128-key steps, 2 one tile / 64-key steps")
     ap.add_argument("--op", default="attention", choices=["attention", "gemm", "gemm_gelu", "softmax"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)

@@ -55,7 +55,7 @@ typedef enum {
     FA_ERR_NULL_PTR = 1,        /* q, k, v, o or lse is NULL for a non-empty problem        */
     FA_ERR_BAD_DIM = 2,         /* B, Sq, Sk < 0, or Sk == 0 while B*Hq*Sq > 0, or too large */
     FA_ERR_HEADS = 3,           /* Hq < 1, Hkv < 1, or Hq % Hkv != 0                         */
-    FA_ERR_UNSUPPORTED_D = 4,   /* D not in {64, 128}                                        */
+    FA_ERR_UNSUPPORTED_D = 4,   /* D not in {64, 128, 256} (or not supported by the chosen kernel) */
     FA_ERR_ALIGN = 5,           /* q/k/v/o not 16-byte aligned, or lse not 4-byte aligned    */
     FA_ERR_ALIAS = 6,           /* o or lse overlaps an input or each other                  */
     FA_ERR_SCALE = 7,           /* scale is NaN or infinite                                  */
@@ -71,7 +71,7 @@ typedef enum {
 
 /*
  * fa_fwd -- bf16 attention forward.  Writes o and lse as described above.
- *   B, Hq, Hkv, Sq, Sk, D : sizes (D in {64, 128}; Hq % Hkv == 0)
+ *   B, Hq, Hkv, Sq, Sk, D : sizes (D in {64, 128, 256}; Hq % Hkv == 0)
  *   causal                : 0 = full attention, 1 = key j allowed iff j <= i (top-left),
  *                           2 = key j allowed iff j <= i + Sk - Sq (bottom-right)
  *   scale                 : multiplies q.k before the softmax (usually 1/sqrt(D))
@@ -84,6 +84,22 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            fa_stream_t stream);
 
 /* fa_fwd_fp16 -- identical to fa_fwd with IEEE fp16 q, k, v and o. */
+/*
+ * fa_fwd_select -- fa_fwd (dtype 0, bf16) / fa_fwd_fp16 (dtype 1) with an explicit kernel
+ * variant, for tuning sweeps (the course's lesson 10: a search space of meta-parameters
+ * measured per workload).  Same results up to rounding order.
+ *   kernel 0: automatic -- 1 for D <= 128, 2 for D = 256 (what fa_fwd does)
+ *   kernel 1: two 128-row query tiles per CTA sharing 128-key steps (D 64 or 128)
+ *   kernel 2: one 128-row query tile per CTA, 64-key steps, double-buffered scores (D 128 or 256;
+ *             the block-size trade of the guide's troubleshooting item, and the only layout
+ *             that fits D = 256 in tensor memory)
+ * An unsupported (kernel, D) pair returns FA_ERR_UNSUPPORTED_D; kernel or dtype out of range
+ * returns FA_ERR_ARG.
+ */
+int fa_fwd_select(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                  fa_stream_t stream, int dtype, int kernel);
+
 int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                 fa_stream_t stream);

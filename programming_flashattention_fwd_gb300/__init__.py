@@ -11,7 +11,8 @@ def __getattr__(name):
     # The CUDA binding is imported lazily so that the input generators can be used on
     # machines without a GPU; any call into the binding loads the library or raises.
     if name in ("fa_fwd", "fa_fwd_fp16", "attention", "fa_strerror", "fa_device_status",
-                "FaError", "load_library", "STATUS", "fa_fwd_debug"):
+                "FaError", "load_library", "STATUS", "fa_fwd_debug", "fa_fwd_select", "gemm",
+                "softmax_rows"):
         from . import binding
         return getattr(binding, name)
     raise AttributeError(name)

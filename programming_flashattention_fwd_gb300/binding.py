@@ -42,6 +42,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = _FWD_ARGS
+    lib.fa_fwd_select.restype = ctypes.c_int
+    lib.fa_fwd_select.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_int]
     lib.fa_fwd_debug.restype = ctypes.c_int
     lib.fa_fwd_debug.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
     lib.fa_strerror.restype = ctypes.c_char_p
@@ -144,14 +146,23 @@ def fa_fwd_debug(q, k, v, o, lse, causal: bool, scale: float, timeout_ns: int = 
           extra=(int(q.dtype == torch.float16), int(timeout_ns), int(inject)))
 
 
-def attention(q, k, v, causal: bool = False, scale: Optional[float] = None,
-              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+def fa_fwd_select(q, k, v, o, lse, causal, scale: float, kernel: int = 0, stream=None) -> None:
+    """The forward with an explicit kernel variant (0 automatic, 1 two query tiles per CTA
+    with 128-key steps, 2 one query tile per CTA with 64-key steps); bf16 or fp16."""
+    _call("fa_fwd_select", q, k, v, o, lse, causal, scale, stream,
+          extra=(int(q.dtype == torch.float16), int(kernel)))
+
+
+def attention(q, k, v, causal=False, scale: Optional[float] = None, stream=None,
+              kernel: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Allocate o and lse on q's device and run the forward; returns (o, lse)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    if q.dtype == torch.float16:
+    if kernel:
+        fa_fwd_select(q, k, v, o, lse, causal, scale, kernel, stream)
+    elif q.dtype == torch.float16:
         fa_fwd_fp16(q, k, v, o, lse, causal, scale, stream)
     else:
         fa_fwd(q, k, v, o, lse, causal, scale, stream)

@@ -33,7 +33,7 @@ def nvcc() -> str:
 
 
 def sources():
-    return [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "gemm_sm103.cu", "softmax_sm103.cu", "fa_api.cpp")]
+    return [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "fa_fwd1_sm103.cu", "gemm_sm103.cu", "softmax_sm103.cu", "fa_api.cpp")]
 
 
 def _stale(path: str) -> bool:
@@ -67,7 +67,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=4) as ex:
+    with ThreadPoolExecutor(max_workers=5) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = out + f".tmp{tag}"
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp, "-cudart", "static"]

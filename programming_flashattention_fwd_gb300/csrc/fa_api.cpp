@@ -44,12 +44,13 @@ bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// 3-D view (D, S, B*H) of a dense [B, H, S, D] 16-bit tensor; 64 x 128 x 1 boxes, 128B swizzle.
-bool encode(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, int D, int S, long long BH)
+// 3-D view (D, S, B*H) of a dense [B, H, S, D] 16-bit tensor; 64 x rows x 1 boxes, 128B swizzle.
+bool encode(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, int D, int S, long long BH,
+            int rows = fa::kBM)
 {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)fa::kBM, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -57,21 +58,30 @@ bool encode(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, int 
     return r == CUDA_SUCCESS;
 }
 
+int check_device();
+
+// kernel: 0 = automatic (two-tile for D <= 128, one-tile for D = 256), 1 = two query tiles per
+// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 128 / 256).
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
-        int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject)
+        int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject,
+        int kernel = 0)
 {
     // ---- argument checks: no CUDA call before these pass
     if (B < 0 || Sq < 0 || Sk < 0) return FA_ERR_BAD_DIM;
     if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_HEADS;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+    if (kernel < 0 || kernel > 2) return FA_ERR_ARG;
+    if (kernel == 0) kernel = (D == 256) ? 2 : 1;
+    if (kernel == 1 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+    if (kernel == 2 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
     if (causal < 0 || causal > 2) return FA_ERR_CAUSAL;
     if (B == 0 || Sq == 0) return FA_OK;
     if (Sk == 0) return FA_ERR_BAD_DIM;
     const long long BHq = (long long)B * Hq, BHkv = (long long)B * Hkv;
-    const long long Tq = (Sq + fa::kBM - 1) / fa::kBM, Tk = (Sk + fa::kBN - 1) / fa::kBN;
+    const int key_tile = kernel == 2 ? 64 : fa::kBN;
+    const long long Tq = (Sq + fa::kBM - 1) / fa::kBM, Tk = (Sk + key_tile - 1) / key_tile;
     const long long NP = (Tq + 1) / 2;
-    if (BHq * NP > 0x7fffffffLL || BHq > 0x7fffffffLL) return FA_ERR_BAD_DIM;
+    if (BHq * Tq > 0x7fffffffLL || BHq > 0x7fffffffLL) return FA_ERR_BAD_DIM;
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return FA_ERR_ALIGN;
@@ -82,26 +92,18 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
         return FA_ERR_ALIAS;
 
     // ---- device
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
-    int st = g_arch_ok[dev].load(std::memory_order_relaxed);
-    if (st == 0) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return FA_ERR_NO_DEVICE;
-        st = (major == 10 && minor == 3) ? 1 : 2;
-        g_arch_ok[dev].store(st, std::memory_order_relaxed);
+    {
+        const int st = check_device();
+        if (st != FA_OK) return st;
     }
-    if (st != 1) return FA_ERR_ARCH;
 
     // ---- TMA descriptors
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return FA_ERR_TENSORMAP;
     fa::Maps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode(enc, &maps.q, q, bf16, D, Sq, BHq) || !encode(enc, &maps.k, k, bf16, D, Sk, BHkv) ||
-        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv))
+    if (!encode(enc, &maps.q, q, bf16, D, Sq, BHq) || !encode(enc, &maps.k, k, bf16, D, Sk, BHkv, key_tile) ||
+        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv, key_tile))
         return FA_ERR_TENSORMAP;
 
     fa::Params p;
@@ -117,7 +119,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.Tk = (int)Tk;
     p.NP = (int)NP;
     p.group = Hq / Hkv;
-    p.num_units = (int)(BHq * NP);
+    p.num_units = (int)(kernel == 2 ? BHq * Tq : BHq * NP);
     // The kernel masks keys with -inf scores and takes the row maximum before scaling, so it
     // needs a positive multiplier: a negative scale negates the scores instead, and a zero
     // scale replaces every score by 0 (uniform weights), both exactly.
@@ -127,7 +129,8 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.timeout_ns = timeout_ns;
     p.inject = inject;
 
-    cudaError_t e = fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = kernel == 2 ? fa::launch_fwd1(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream))
+                                : fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -242,6 +245,13 @@ int fa_fwd_debug(const void *q, const void *k, const void *v, void *o, float *ls
     return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, is_fp16 == 0, timeout_ns, inject);
 }
 
+int fa_fwd_select(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                  int Sk, int D, int causal, float scale, fa_stream_t stream, int dtype, int kernel)
+{
+    if (dtype != 0 && dtype != 1) return FA_ERR_ARG;
+    return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, dtype == 0, 0, 0, kernel);
+}
+
 const char *fa_strerror(int status)
 {
     switch (status) {
@@ -249,7 +259,7 @@ const char *fa_strerror(int status)
     case FA_ERR_NULL_PTR: return "FA_ERR_NULL_PTR: a tensor pointer is NULL";
     case FA_ERR_BAD_DIM: return "FA_ERR_BAD_DIM: negative size, Sk == 0 for a non-empty problem, or problem too large";
     case FA_ERR_HEADS: return "FA_ERR_HEADS: Hq and Hkv must be >= 1 with Hq % Hkv == 0";
-    case FA_ERR_UNSUPPORTED_D: return "FA_ERR_UNSUPPORTED_D: head dimension D must be 64 or 128";
+    case FA_ERR_UNSUPPORTED_D: return "FA_ERR_UNSUPPORTED_D: D must be 64, 128 or 256 (and supported by the selected kernel)";
     case FA_ERR_ALIGN: return "FA_ERR_ALIGN: q/k/v/o must be 16-byte aligned and lse 4-byte aligned";
     case FA_ERR_ALIAS: return "FA_ERR_ALIAS: o or lse overlaps an input or each other";
     case FA_ERR_SCALE: return "FA_ERR_SCALE: scale is NaN or infinite";
@@ -269,8 +279,10 @@ int fa_device_status(fa_stream_t stream, uint32_t *detail)
 {
     uint32_t w = 0, wg = 0;
     if (fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &w) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    uint32_t w1 = 0;
     if (fa::read_and_clear_gemm_status(&wg) != cudaSuccess) return FA_ERR_NO_DEVICE;
-    if (!(w & 1u)) w = wg;   // first expiry wins; attention's word is checked first
+    if (fa::read_and_clear_fa1_status(&w1) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    if (!(w & 1u)) w = (w1 & 1u) ? w1 : wg;   // first expiry wins, attention kernels checked first
     if (detail) *detail = w;
     return (w & 1u) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }

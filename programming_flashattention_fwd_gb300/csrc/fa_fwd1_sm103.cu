@@ -1,0 +1,495 @@
+// fa_fwd1_sm103.cu -- FlashAttention forward, one query tile per CTA, 64-key tiles, with
+// double-buffered scores in tensor memory: the variant for head dimension 256 (and a 64-key
+// alternative for D = 128).  Same computation as fa_fwd_sm103.cu (the flash-attention
+// section of "Guia Prático de Programação de GPU com Tiles"; the FlashAttention-4 features of
+// "Como Domar o Blackwell Sem Enlouquecer com CUDA"); the guide's troubleshooting item trades
+// the 128-row block for 64 to save memory, which is what the key tile does here.
+//
+// With D = 256 the two-tile layout of the main kernel no longer fits in TMEM (2 x 128 score
+// columns + 2 x 256 accumulator columns > 512).  Instead one 128-row query tile owns
+//   S_0 [0,64)  S_1 [64,128)   fp32 scores of two consecutive key tiles; P (16-bit pairs)
+//                              overwrites the first 32 columns of its S
+//   O   [128, 128+D)           fp32 accumulator
+// and the MMA warp computes S(j+1) = Q K_{j+1}^T while the softmax works on S(j); then
+// O += P(j) V_j.  Per 64-key step the tensor pipe has 2 x 128*64*D multiply-adds (1024 cycles
+// at D = 256), which the softmax of 64 keys per row fits under.
+//
+//   warp 0       TMA producer of K / V tiles in the order the MMAs consume them (K_0, K_1,
+//                V_0, K_2, V_1, ...), into a ring of 64-row slots
+//   warp 1       TMEM owner and MMA issuer (whole warp; one elected lane issues)
+//   warp 2       TMA producer of query tiles into two rotating buffers
+//   warps 4-7    softmax / lazy correction / epilogue, one thread per query row
+//
+// The softmax consumes every P V completion in order: before publishing P(j) it waits for
+// P V(j-1) (already done in the steady state), so O can be rescaled safely; the epilogue waits
+// for the last one.  Every wait is bounded, as in the main kernel.
+#include <atomic>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+#include "watchdog.cuh"
+
+namespace fa {
+
+__device__ unsigned int g_fa1_status;
+
+namespace one {
+
+constexpr int BM = 128, BN = 64;
+constexpr int THREADS = 256;
+constexpr float kTau = 8.0f;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+enum Site : uint32_t { S_EMPTY = 1, S_Q = 2, S_FULL = 3, S_P = 4, S_S = 5, S_PV = 6, S_DRAIN = 7, S_QFREE = 8, S_SMEM = 9 };
+
+template <int D>
+struct Cfg {
+    static constexpr int QTILE = BM * D * 2;       // 128 rows
+    static constexpr int KVTILE = BN * D * 2;      // 64 rows
+    static constexpr int PANELS = D / 64;
+    static constexpr int QPANEL = BM * 128;        // 16 KB
+    static constexpr int KVPANEL = BN * 128;       // 8 KB
+    static constexpr int NQ = 2;
+    static constexpr int NS = (D == 256) ? 3 : 8;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_RING = NQ * QTILE;
+    static constexpr int OFF_BAR = OFF_RING + NS * KVTILE;
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 1 + 1 + 1;   // q, qfree, full, empty, S[2], P, PV, done
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int ALLOC = (BYTES + 1024 <= 232448) ? BYTES + 1024 : 232448;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
+};
+
+struct Unit {
+    int zq, zkv, t, nk;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long g = (long long)round * G + ((round & 1) ? (G - 1 - c) : c);
+    if (g >= p.num_units) return false;
+    int bh, t;
+    if (CAUSAL) {   // heaviest query tiles first
+        const int nbh = p.B * p.Hq;
+        t = p.Tq - 1 - (int)(g / nbh);
+        bh = (int)(g % nbh);
+    } else {
+        bh = (int)(g / p.Tq);
+        t = (int)(g % p.Tq);
+    }
+    const int b = bh / p.Hq, hq = bh % p.Hq;
+    u.zq = b * p.Hq + hq;
+    u.zkv = b * p.Hkv + hq / p.group;
+    u.t = t;
+    if (!CAUSAL) {
+        u.nk = p.Tk;
+    } else {
+        const long long hi = (long long)t * BM + (BM - 1) + p.coff;
+        u.nk = hi < 0 ? 0 : (int)min((long long)p.Tk, hi / BN + 1);
+    }
+    return true;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(THREADS, 1)
+    fa_fwd1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sb = raw + pad;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t sQ = sb + C::OFF_Q, sRing = sb + C::OFF_RING, bar0 = sb + C::OFF_BAR;
+    auto bar_q = [&](int i) { return bar0 + 8u * i; };
+    auto bar_qfree = [&](int i) { return bar0 + 8u * (C::NQ + i); };
+    auto bar_full = [&](int s) { return bar0 + 8u * (2 * C::NQ + s); };
+    auto bar_empty = [&](int s) { return bar0 + 8u * (2 * C::NQ + C::NS + s); };
+    const uint32_t barS = bar0 + 8u * (2 * C::NQ + 2 * C::NS);   // + 8 * buffer
+    const uint32_t barP = barS + 16u, barPV = barS + 24u, barDone = barS + 32u;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    unsigned int *status = &g_fa1_status;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (pad + (uint32_t)C::BYTES > dynamic_smem_size_u32()) {
+        if (threadIdx.x == 0) atomicOr(status, 1u | (S_SMEM << 8));
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NQ; ++i) {
+            mbar_init(bar_q(i), 1);
+            mbar_init(bar_qfree(i), 1);
+        }
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
+        }
+        mbar_init(barS, 1);
+        mbar_init(barS + 8, 1);
+        mbar_init(barP, 4);
+        mbar_init(barPV, 1);
+        mbar_init(barDone, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ K/V producer (consumption order)
+        if (lane == 0) {
+            int use = 0;
+            bool ok = true;
+            auto load = [&](const CUtensorMap *m, int j, int zkv) {
+                const int s = use % C::NS;
+                if (!bounded_wait(bar_empty(s), ((use / C::NS) & 1) ^ 1, abort_flag, tmo, S_EMPTY, status))
+                    return false;
+                mbar_arrive_expect_tx(bar_full(s), C::KVTILE);
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d(sRing + s * C::KVTILE + pn * C::KVPANEL, m, pn * 64, j * BN, zkv, bar_full(s));
+                ++use;
+                return true;
+            };
+            Unit u;
+            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+                if (u.nk == 0) continue;
+                ok = load(&tmK, 0, u.zkv);
+                for (int j = 0; j < u.nk && ok; ++j) {
+                    if (j + 1 < u.nk) ok = load(&tmK, j + 1, u.zkv);
+                    if (ok) ok = load(&tmV, j, u.zkv);
+                }
+            }
+            for (int x = max(0, use - C::NS); x < use; ++x)
+                bounded_wait(bar_full(x % C::NS), (x / C::NS) & 1, abort_flag, tmo, S_DRAIN, status, false);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ Q producer
+        if (lane == 0) {
+            int tau = 0;
+            bool ok = true;
+            Unit u;
+            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+                if (u.nk == 0) continue;
+                const int buf = tau % C::NQ;
+                if (tau >= C::NQ &&
+                    !bounded_wait(bar_qfree(buf), ((tau / C::NQ) - 1) & 1, abort_flag, tmo, S_QFREE, status))
+                    break;
+                mbar_arrive_expect_tx(bar_q(buf), C::QTILE);
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d(sQ + buf * C::QTILE + pn * C::QPANEL, &tmQ, pn * 64, u.t * BM, u.zq, bar_q(buf));
+                ++tau;
+            }
+            for (int x = max(0, tau - C::NQ); x < tau; ++x)
+                bounded_wait(bar_q(x % C::NQ), (x / C::NQ) & 1, abort_flag, tmo, S_DRAIN, status, false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (whole warp)
+        constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false);
+        constexpr uint32_t idPV = idesc_f16(BF16, BM, D, true);
+        constexpr uint32_t HI = sdesc_hi_sw128(1024);
+        auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) {
+            return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_flag, tmo, site, status));
+        };
+        // S = Q K^T over D (both K-major, 16 columns of D per instruction)
+        auto issue_s = [&](uint32_t dS, uint32_t sQt, uint32_t sK) {
+            const uint32_t qlo = sdesc_lo(sQt, 16), klo = sdesc_lo(sK, 16);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss_elect(dS, qlo + (uint32_t)(((kk >> 2) * C::QPANEL + (kk & 3) * 32) >> 4),
+                             klo + (uint32_t)(((kk >> 2) * C::KVPANEL + (kk & 3) * 32) >> 4), HI, idS, kk > 0);
+        };
+        // O += P V over 64 keys: A = P from TMEM, B = V (MN-major, 64-column panels 8 KB apart)
+        auto issue_pv = [&](uint32_t tP, uint32_t sV, bool first) {
+            const uint32_t vlo = sdesc_lo(sV, C::KVPANEL);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts_elect(tmem + C::COL_O, tP + kk * 8, vlo + (uint32_t)((kk * 2048) >> 4), HI, idPV,
+                             (first && kk == 0) ? 0u : 1u);
+        };
+        auto tS = [&](uint32_t gs) { return tmem + ((gs & 1) ? C::COL_S1 : C::COL_S0); };
+        int use = 0, tau = 0;
+        uint32_t g = 0;   // global key step: S buffer g % 2, barS phase (g / 2) & 1, barP / barPV phase g & 1
+        bool ok = true;
+        Unit u;
+        for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+            if (u.nk == 0) continue;
+            const int buf = tau % C::NQ;
+            ok = wait_u(bar_q(buf), (tau / C::NQ) & 1, S_Q);
+            ++tau;
+            const uint32_t sQt = sQ + buf * C::QTILE;
+            if (ok) ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(tS(g), sQt, sRing + (use % C::NS) * C::KVTILE);
+            tc_commit_elect(barS + 8u * (g & 1));
+            if (u.nk == 1) tc_commit_elect(bar_qfree(buf));
+            tc_commit_elect(bar_empty(use % C::NS));
+            ++use;
+            for (int j = 0; j < u.nk && ok; ++j) {
+                const uint32_t gs = g + j;
+                if (j + 1 < u.nk) {
+                    ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(tS(gs + 1), sQt, sRing + (use % C::NS) * C::KVTILE);
+                    tc_commit_elect(barS + 8u * ((gs + 1) & 1));
+                    if (j + 2 == u.nk) tc_commit_elect(bar_qfree(buf));
+                    tc_commit_elect(bar_empty(use % C::NS));
+                    ++use;
+                }
+                ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL) && wait_u(barP, gs & 1, S_P);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(tS(gs), sRing + (use % C::NS) * C::KVTILE, j == 0);
+                tc_commit_elect(barPV);
+                tc_commit_elect(bar_empty(use % C::NS));
+                ++use;
+            }
+            g += u.nk;
+        }
+        tc_commit_elect(barDone);
+        bounded_wait(barDone, 0, abort_flag, tmo, S_DRAIN, status, false);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / correction / epilogue
+        const int r = threadIdx.x - 128;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tO = tmem + lane_off + C::COL_O;
+        const float sl2 = p.sl2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        uint32_t g = 0;
+        bool ok = true;
+        Unit u;
+        for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+            const int row = u.t * BM + r;
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)u.zq * p.Sq + row) * (size_t)(D * 2);
+            if (u.nk == 0) {   // no allowed key for any row of this tile: o = 0, lse = -inf
+                if (row < p.Sq) {
+#pragma unroll 4
+                    for (int c = 0; c < D * 2; c += 16) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
+                    p.lse[(size_t)u.zq * p.Sq + row] = -INFINITY;
+                }
+                continue;
+            }
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < u.nk; ++j) {
+                const uint32_t gs = g + j;
+                const uint32_t tSb = tmem + lane_off + ((gs & 1) ? C::COL_S1 : C::COL_S0);
+                ok = __all_sync(0xffffffffu, bounded_wait(barS + 8u * (gs & 1), (gs >> 1) & 1, abort_flag, tmo, S_S, status));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sv[BN];
+                {
+                    uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 0);
+                    uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32);
+                    tmem_ld_x32(tSb + 0, v0);
+                    tmem_ld_x32(tSb + 32, v1);
+                    tmem_wait_ld();
+                    reg_fence_x32(v0);
+                    reg_fence_x32(v1);
+                }
+                float *s = reinterpret_cast<float *>(sv);
+                if (p.smode == 1) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) s[c] = -s[c];
+                } else if (p.smode == 2) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) s[c] = 0.f;
+                }
+                const int kbase = j * BN;
+                const bool tail = kbase + BN > p.Sk;
+                const bool diag = CAUSAL && (kbase + BN - 1 > u.t * BM + p.coff);
+                if (tail || diag) {
+                    int lim = p.Sk - 1 - kbase;
+                    if (CAUSAL) lim = min(lim, row + p.coff - kbase);
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c > lim) s[c] = -INFINITY;
+                }
+                // row maximum: eight chains seeded with 16 scores, then 3 rounds of 16 (== 64)
+                static_assert(BN == 64, "row-max chains cover 64 scores");
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                for (int c = 16; c + 16 <= BN; c += 16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+                }
+                const float mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+                const float m_new = fmaxf(m_used, mrow * sl2);
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_used = m_new;
+                } else if (m_new - m_used > kTau) {
+                    alpha = ex2_approx(m_used - m_new);
+                    l *= alpha;
+                    m_used = m_new;
+                    rescale = true;
+                }
+                const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+                const uint64_t negm2 = f2_pack(-msub, -msub);
+                uint64_t lsum2[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lsum2[i] = f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int i = 32 * c + 2 * e;
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(s[i], s[i + 1]), sl2x2, negm2), t0, t1);
+                        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                        lsum2[e & 7] = f2_add(lsum2[e & 7], f2_pack(p0, p1));
+                        pk[e] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st_x16(tSb + 16 * c, pk);
+                }
+                // P V(j-1) must be complete before O may be rescaled (and it is consumed here
+                // in every step, keeping the completion count in step with the MMA warp)
+                if (j > 0) {
+                    ok = __all_sync(0xffffffffu, bounded_wait(barPV, (gs - 1) & 1, abort_flag, tmo, S_PV, status));
+                    if (!ok) break;
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        tc_fence_after();
+                        const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t ov[32];
+                            tmem_ld_x32(tO + c, ov);
+                            tmem_wait_ld();
+                            reg_fence_x32(ov);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                float lo, hi;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2), lo, hi);
+                                ov[e] = __float_as_uint(lo);
+                                ov[e + 1] = __float_as_uint(hi);
+                            }
+                            tmem_st_x32(tO + c, ov);
+                        }
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(barP);
+                const uint64_t q0 = f2_add(f2_add(lsum2[0], lsum2[1]), f2_add(lsum2[2], lsum2[3]));
+                const uint64_t q1 = f2_add(f2_add(lsum2[4], lsum2[5]), f2_add(lsum2[6], lsum2[7]));
+                float la, lb;
+                f2_unpack(f2_add(q0, q1), la, lb);
+                l += la + lb;
+            }
+            if (!ok) break;
+            // epilogue: the last P V of this tile, then O / l -> 16-bit rows, and the lse
+            ok = __all_sync(0xffffffffu, bounded_wait(barPV, (g + u.nk - 1) & 1, abort_flag, tmo, S_PV, status));
+            if (!ok) break;
+            g += u.nk;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const uint64_t il2 = f2_pack(inv_l, inv_l);
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t ov[32];
+                tmem_ld_x32(tO + c, ov);
+                tmem_wait_ld();
+                reg_fence_x32(ov);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float lo, hi;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), il2), lo, hi);
+                    pk[e] = pack2<BF16>(lo, hi);
+                }
+                if (row < p.Sq) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        st_global_v4(orow + c * 2 + q4 * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                }
+            }
+            if (row < p.Sq) {
+                const float lse = l > 0.f ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+                p.lse[(size_t)u.zq * p.Sq + row] = lse;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t stream)
+{
+    auto kern = fa_fwd1_kernel<D, BF16, CAUSAL>;
+    static std::atomic<uint64_t> configured{0};
+    static std::atomic<int> sm_count[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::ALLOC);
+        if (e != cudaSuccess) return e;
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        sm_count[dev].store(nsm, std::memory_order_relaxed);
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    Params q = p;
+    if (q.timeout_ns == 0) q.timeout_ns = kDefaultTimeoutNs;
+    const int grid = min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
+    kern<<<grid, THREADS, Cfg<D>::ALLOC, stream>>>(m.q, m.k, m.v, q);
+    return cudaGetLastError();
+}
+
+} // namespace one
+
+cudaError_t launch_fwd1(int D, bool bf16, bool causal, const Maps &m, const Params &p, cudaStream_t st)
+{
+#define F1_CASE(DD, BB, CC) \
+    if (D == DD && bf16 == BB && causal == CC) return one::launch_one<DD, BB, CC>(m, p, st);
+    F1_CASE(128, true, false) F1_CASE(128, true, true) F1_CASE(128, false, false) F1_CASE(128, false, true)
+    F1_CASE(256, true, false) F1_CASE(256, true, true) F1_CASE(256, false, false) F1_CASE(256, false, true)
+#undef F1_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_fa1_status(uint32_t *word)
+{
+    unsigned int w = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&w, g_fa1_status, sizeof(w));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_fa1_status, &zero, sizeof(zero));
+    if (word) *word = w;
+    return e;
+}
+
+} // namespace fa

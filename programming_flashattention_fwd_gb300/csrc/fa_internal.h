@@ -38,6 +38,11 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const Maps &maps, const Pa
 // Reads and clears the current device's watchdog word (synchronous on `stream`).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word);
 
+// One query tile per CTA, 64-key steps, double-buffered scores (D = 128 or 256).  K/V maps
+// use 64-row boxes; Params.Tk counts 64-key tiles and num_units = B * Hq * Tq.
+cudaError_t launch_fwd1(int D, bool bf16, bool causal, const Maps &maps, const Params &p, cudaStream_t stream);
+cudaError_t read_and_clear_fa1_status(uint32_t *word);
+
 // ---------------------------------------------------------------- tiled matrix product
 struct GemmParams {
     void *c;               // [M, N] row-major, 16-bit (input type) or fp32

@@ -85,6 +85,16 @@ WORKLOADS: Dict[str, Workload] = {
     ]
 }
 
+# Head dimension 256 (the tile-size / head-dimension variants): the same GQA causal shape and a
+# non-causal one, served by the one-query-tile kernel.
+EXTRA_WORKLOADS: Dict[str, Workload] = {
+    w.name: w for w in [
+        Workload("gqa_causal_b2_h32kv8_s4096_d256", 2, 32, 8, 4096, 4096, 256, "bf16", True, 12),
+        Workload("mha_b4_h16_s2048_d256", 4, 16, 16, 2048, 2048, 256, "bf16", False, 13),
+    ]
+}
+ALL_WORKLOADS: Dict[str, Workload] = {**WORKLOADS, **EXTRA_WORKLOADS}
+
 # The workload the benchmark times by default (GQA, causal, D=128, 275 GFLOP per call).
 DEFAULT_BENCH_WORKLOAD = "gqa_causal_b2_h32kv8_s4096"
 
@@ -128,4 +138,5 @@ def sample_rows(w: Workload, n: int = 256, seed: Optional[int] = None,
     return np.asarray(uniq, dtype=np.int64).reshape(-1, 3)
 
 
-__all__ = ["Workload", "WORKLOADS", "DEFAULT_BENCH_WORKLOAD", "make_qkv", "sample_rows"]
+__all__ = ["Workload", "WORKLOADS", "EXTRA_WORKLOADS", "ALL_WORKLOADS", "DEFAULT_BENCH_WORKLOAD", "make_qkv",
+           "sample_rows"]

@@ -36,7 +36,7 @@ def declared_status_codes():
 def test_header_declares_the_entry_points():
     fns = declared_functions()
     for name in ("fa_fwd", "fa_fwd_fp16", "fa_strerror", "fa_device_status", "fa_fwd_debug", "fa_gemm",
-                 "fa_softmax_rows"):
+                 "fa_softmax_rows", "fa_fwd_select"):
         assert name in fns
 
 
@@ -72,7 +72,7 @@ def call(lib, fn="fa_fwd", q=Q, k=K, v=V, o=O, lse=L, **over):
 @pytest.mark.parametrize("over,code", [
     (dict(B=-1), 2), (dict(Sq=-5), 2), (dict(Sk=-1), 2), (dict(Sk=0), 2),
     (dict(Hq=0), 3), (dict(Hkv=0), 3), (dict(Hq=6, Hkv=4), 3), (dict(Hq=2, Hkv=4), 3),
-    (dict(D=32), 4), (dict(D=96), 4), (dict(D=256), 4),
+    (dict(D=32), 4), (dict(D=96), 4), (dict(D=192), 4), (dict(D=512), 4),
     (dict(scale=math.nan), 7), (dict(scale=math.inf), 7),
     (dict(B=100000, Hq=100000, Hkv=1), 2),
     (dict(causal=3), 13), (dict(causal=-1), 13),
@@ -150,3 +150,18 @@ def test_gemm_empty_and_bias_optional(lib):
 def test_softmax_invalid_arguments(lib, args, code):
     x, y, rows, cols, dtype = args
     assert lib.fa_softmax_rows(x, y, rows, cols, dtype, None) == code
+
+
+@pytest.mark.parametrize("D,dtype,kernel,code", [
+    (128, 0, 3, 15), (128, 2, 1, 15), (128, 0, -1, 15),
+    (256, 0, 1, 4), (64, 1, 2, 4), (192, 0, 0, 4),
+])
+def test_select_invalid_arguments(lib, D, dtype, kernel, code):
+    assert lib.fa_fwd_select(Q, K, V, O, L, 1, 4, 2, 256, 256, D, 1, 0.1, None, dtype, kernel) == code
+
+
+def test_select_valid_pairs_pass_validation(lib):
+    # every supported (kernel, D) pair gets past validation: an overlapping lse makes each
+    # call stop at the overlap check instead, before any CUDA call
+    for kernel, D in ((0, 64), (0, 128), (0, 256), (1, 64), (1, 128), (2, 128), (2, 256)):
+        assert lib.fa_fwd_select(Q, K, V, O, O + 16, 1, 4, 2, 256, 256, D, 1, 0.1, None, 0, kernel) == 6

@@ -26,7 +26,7 @@ import torch
 
 import oracle
 from programming_flashattention_fwd_gb300 import build as fa_build
-from programming_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, make_qkv, sample_rows
+from programming_flashattention_fwd_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS, Workload, make_qkv, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -42,15 +42,18 @@ def fa():
     return binding
 
 
-def run_gpu(fa, w: Workload, q, k, v, poison=True):
+def run_gpu(fa, w: Workload, q, k, v, poison=True, kernel=0):
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o = torch.empty_like(qd)
     lse = torch.empty(qd.shape[:3], dtype=torch.float32, device="cuda")
     if poison:
         o.fill_(float("nan"))
         lse.fill_(float("nan"))
-    fn = fa.fa_fwd_fp16 if w.is_fp16 else fa.fa_fwd
-    fn(qd, kd, vd, o, lse, w.causal, w.softmax_scale)
+    if kernel:
+        fa.fa_fwd_select(qd, kd, vd, o, lse, w.causal, w.softmax_scale, kernel)
+    else:
+        fn = fa.fa_fwd_fp16 if w.is_fp16 else fa.fa_fwd
+        fn(qd, kd, vd, o, lse, w.causal, w.softmax_scale)
     torch.cuda.synchronize()
     st, word = fa.fa_device_status()
     assert st == 0, f"watchdog fired (word {word:#x})"
@@ -71,9 +74,9 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert lerr.max() <= LSE_ABS, f"{what}: max |dlse| = {lerr.max():.3e}"
 
 
-@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("name", list(WORKLOADS) + list(EXTRA_WORKLOADS))
 def test_workload_parity(fa, orc, name):
-    w = WORKLOADS[name]
+    w = {**WORKLOADS, **EXTRA_WORKLOADS}[name]
     q, k, v = make_qkv(w)
     o, lse = run_gpu(fa, w, q, k, v)
     assert torch.isfinite(o).all().item(), "some output rows were never written"
@@ -106,6 +109,41 @@ def test_shape_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
     o, lse = run_gpu(fa, w, q, k, v)
     o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
     check(o, lse, o_ref, l_ref, f"{w}")
+
+
+SWEEP_ONE = []
+for D in (128, 256):
+    for (B, Hq, Hkv, Sq, Sk) in [(1, 1, 1, 1, 1), (1, 2, 1, 63, 63), (1, 2, 2, 64, 65), (2, 4, 2, 129, 129),
+                                 (1, 3, 3, 300, 300), (1, 4, 2, 384, 200), (1, 2, 1, 200, 384),
+                                 (1, 2, 1, 513, 100), (1, 2, 2, 1, 300)]:
+        for causal in (0, 1, 2):
+            SWEEP_ONE.append((B, Hq, Hkv, Sq, Sk, D, causal))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal", SWEEP_ONE)
+def test_one_tile_kernel_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
+    """The one-query-tile kernel (64-key steps): D = 256 through the automatic choice, D = 128
+    through fa_fwd_select(kernel=2); every row checked."""
+    seed = zlib.crc32(repr(("one", B, Hq, Hkv, Sq, Sk, D, causal, dtype)).encode()) % 100000
+    w = Workload("sweep1", B, Hq, Hkv, Sq, Sk, D, dtype, causal, seed,
+                 q_std=2.0 if dtype == "fp16" else 1.0, k_std=2.0 if dtype == "fp16" else 1.0)
+    q, k, v = make_qkv(w)
+    o, lse = run_gpu(fa, w, q, k, v, kernel=0 if D == 256 else 2)
+    o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
+    check(o, lse, o_ref, l_ref, f"{w}")
+
+
+def test_kernel_variants_agree_at_d128(fa, orc):
+    """Both kernels serve D = 128: each matches the oracle on the bench shape's rows."""
+    w = WORKLOADS["gqa_causal_b2_h32kv8_s4096"]
+    q, k, v = make_qkv(w)
+    rows = sample_rows(w, n=128)
+    o_ref, l_ref = orc.rows(q, k, v, False, w.causal, w.softmax_scale, rows)
+    r = torch.from_numpy(rows)
+    for kernel in (1, 2):
+        o, lse = run_gpu(fa, w, q, k, v, kernel=kernel)
+        check(o.cpu()[r[:, 0], r[:, 1], r[:, 2]], lse.cpu()[r[:, 0], r[:, 1], r[:, 2]], o_ref, l_ref, f"kernel {kernel}")
 
 
 def test_bottom_right_prefill(fa, orc):
