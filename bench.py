@@ -7,8 +7,10 @@ A step is one fa_fwd call over the whole workload (every query row of every head
 ``value`` is attention TFLOP/s (4*B*Hq*Sq*Sk*D, halved when causal) over the K timed steps,
 timed with CUDA events on the launching stream with the inputs resident in HBM; the L2 is
 flushed (a 256 MiB write) between timed steps, outside the events.  ``e2e`` is the same
-metric through the public Python binding with pinned host buffers: every step copies q, k, v
-host->device, runs the call and copies o and lse back, all inside the events.
+metric through the host-memory entry point (fa_fwd_host) on pinned host buffers: every step
+copies q, k, v host->device, runs the attention and copies o and lse back, all inside the
+events, with the copies of one chunk of heads overlapped with the kernels of another
+(``--chunks`` sets the pipeline depth).
 
 ``roofline`` compares the kernel against the measured dense bf16 tensor peak of the pool's
 GB300s (MEASURED_PEAKS.json when present, else the fallback figure, as stated in the line).
@@ -52,15 +54,33 @@ PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
 
 
 # ----------------------------------------------------------------------------- helpers
-def kernel_source_hash() -> str:
-    """sha256 of the CUDA sources: ties an ncu traffic figure to the kernel it measured."""
+# The sources each timed kernel is built from: its own translation unit plus the shared
+# device headers and the host code that encodes its tensor maps and launch shape.
+COMMON_SOURCES = ("ptx.cuh", "watchdog.cuh", "fa_internal.h", "fa_api.cpp")
+KERNEL_SOURCES = {
+    "fa::fa_fwd_kernel": ("fa_fwd_sm103.cu",),
+    "fa::fa_fwd1_kernel": ("fa_fwd1_sm103.cu",),
+    "fa::gemm::gemm_kernel": ("gemm_sm103.cu",),
+    "fa::sm::softmax_regs_kernel": ("softmax_sm103.cu",),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 of the sources `kernel` is built from: ties an ncu traffic figure to the code it
+    measured (a change to another kernel leaves it valid)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "programming_flashattention_fwd_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in sorted(KERNEL_SOURCES[kernel] + COMMON_SOURCES):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def attention_kernel(w, kernel: int) -> str:
+    """The kernel fa_fwd_select runs for this workload and variant (0 = automatic)."""
+    k = kernel or (2 if w.D == 256 else 1)
+    return "fa::fa_fwd1_kernel" if k == 2 else "fa::fa_fwd_kernel"
 
 
 def measured_peaks():
@@ -81,17 +101,18 @@ def measured_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(workload: str):
-    """Per-launch DRAM bytes from a committed ncu summary for this workload and this exact
-    kernel source (a line 'traffic_bytes_per_launch: N' next to 'kernel_source_sha: H'),
-    else None."""
-    want = kernel_source_hash()
+def ncu_traffic(workload: str, kernel: str):
+    """Per-launch DRAM bytes from a committed ncu summary of `kernel` on this workload and
+    this exact kernel source (lines 'kernel: K', 'workload: W', 'kernel_source_sha: H' and
+    'traffic_bytes_per_launch: N'), else None."""
+    want = kernel_source_hash(kernel)
     for p in sorted(glob.glob(PROFILE_GLOB)):
-        txt = open(p).read()
-        if f"workload: {workload}" not in txt or f"kernel_source_sha: {want}" not in txt:
+        lines = [ln.strip() for ln in open(p).read().splitlines()]
+        if (f"workload: {workload}" not in lines or f"kernel_source_sha: {want}" not in lines
+                or f"kernel: {kernel}" not in lines):
             continue
-        for line in txt.splitlines():
-            if line.strip().startswith("traffic_bytes_per_launch:"):
+        for line in lines:
+            if line.startswith("traffic_bytes_per_launch:"):
                 try:
                     return float(line.split(":", 1)[1])
                 except ValueError:
@@ -338,12 +359,16 @@ def run_ours(args, w, world, rank, local):
     l2 = torch.empty_like(lse)
 
     def e2e_step():
-        q2.copy_(q_p, non_blocking=True)
-        k2.copy_(k_p, non_blocking=True)
-        v2.copy_(v_p, non_blocking=True)
-        fn(q2, k2, v2, o2, l2, w.causal, w.softmax_scale)
-        o_p.copy_(o2, non_blocking=True)
-        l_p.copy_(l2, non_blocking=True)
+        if args.kernel:   # an explicit variant: copies in, the kernel, copies back, one after another
+            q2.copy_(q_p, non_blocking=True)
+            k2.copy_(k_p, non_blocking=True)
+            v2.copy_(v_p, non_blocking=True)
+            fn(q2, k2, v2, o2, l2, w.causal, w.softmax_scale)
+            o_p.copy_(o2, non_blocking=True)
+            l_p.copy_(l2, non_blocking=True)
+        else:             # the host-memory entry point: copies and kernels overlapped chunk by chunk
+            binding.fa_fwd_host(q_p, k_p, v_p, o_p, l_p, q2, k2, v2, o2, l2, w.causal, w.softmax_scale,
+                                chunks=args.chunks, stream=stream)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -365,7 +390,8 @@ def run_ours(args, w, world, rank, local):
     flops = w.flops()
     peak, peak_sus, peak_src = measured_peaks()
     achieved = flops / t_step / 1e12
-    traffic = ncu_traffic(w.name)
+    kname = attention_kernel(w, args.kernel)
+    traffic = ncu_traffic(w.name, kname)
     line = {
         "metric": METRIC, "value": flops * world / t_step / 1e12, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -379,7 +405,7 @@ def run_ours(args, w, world, rank, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} dense bf16 (burst)" + (
                          f"; sustained {peak_sus}" if peak_sus else ""),
-                     "kernel": "fa::fa_fwd_kernel"},
+                     "kernel": kname},
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -490,6 +516,7 @@ def run_op(args, world, rank, local):
     if rank != 0:
         return
 
+    kname = "fa::gemm::gemm_kernel" if bound == "tensor" else "fa::sm::softmax_regs_kernel"
     if bound == "tensor":
         peak, _, src = measured_peaks()
         peak_unit = "TFLOP/s"
@@ -522,9 +549,9 @@ def run_op(args, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": args.steps,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": peak_unit,
-                     "frac": achieved / peak, "traffic": ncu_traffic(name),
+                     "frac": achieved / peak, "traffic": ncu_traffic(name, kname),
                      "peak_source": f"{src}" + (" dense bf16 (burst)" if bound == "tensor" else " HBM copy"),
-                     "kernel": "fa::gemm::gemm_kernel" if bound == "tensor" else "fa::sm::softmax_regs_kernel"},
+                     "kernel": kname},
         "clocks": clocks,
     }
     if cpu_work is not None:
@@ -547,6 +574,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
                     help="attention kernel variant: 0 automatic, 1 two tiles / 128-key steps, 2 one tile / 64-key steps")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="pipeline depth of the host-memory (e2e) call; 0 = the library's default")
     ap.add_argument("--op", default="attention", choices=["attention", "gemm", "gemm_gelu", "softmax"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)

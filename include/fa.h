@@ -148,6 +148,40 @@ int fa_gemm(const void *a, const void *b, void *c, const float *bias, int M, int
             int dtype, int out_fp32, int epilogue, fa_stream_t stream);
 
 /*
+ * fa_fwd_host -- the attention forward of fa_fwd / fa_fwd_fp16 for q, k, v in HOST memory,
+ * with o and lse written back to host memory: the copies in, the kernels and the copies
+ * back are overlapped chunk by chunk.  The pages define no host-memory entry point; this is
+ * the host-side wrapper that the tile course's lesson 5 asks for (launch, memory safety,
+ * input checks) with the overlap of data movement and computation that its "real use
+ * cases" list names, applied to the host<->device link.
+ *   q_h, k_h, v_h   host inputs, same layout as fa_fwd's q, k, v; read only.  Pinned
+ *                   (page-locked) memory gives the overlap; pageable memory is accepted but
+ *                   each copy then blocks the host.
+ *   o_h, lse_h      host outputs, layout of o and lse
+ *   q_d .. lse_d    caller-owned DEVICE buffers of the same sizes on the current device: the
+ *                   staging area that the copies fill (q_d, k_d, v_d) and the kernels write
+ *                   (o_d, lse_d); on return of the work they hold the inputs and results.
+ *   B .. scale      as for fa_fwd;  dtype 0 = bf16, 1 = fp16
+ *   chunks          pipeline depth: the flat (batch, KV head) axis is cut into this many
+ *                   runs (0 = automatic, 4; capped at B * Hkv; at most 64)
+ *   stream          the work starts after what is already enqueued on `stream`, and `stream`
+ *                   waits for the last copy back: synchronise it before reading o_h / lse_h.
+ * The call is asynchronous and uses three internal streams per device, created on its first
+ * call for that device.  Calls for one device are enqueued one at a time (a lock); two calls
+ * on different caller streams that share buffers race, as any two kernels would.
+ * Results are bit-identical to fa_fwd on the same inputs (each output row is computed by the
+ * same kernel in the same order).  Argument errors (fa_fwd's checks on the device buffers,
+ * NULL host pointers, any overlap between a written range and another range, dtype or chunks
+ * out of range) are returned before any CUDA call; a CUDA error after the first copy was
+ * enqueued returns FA_ERR_LAUNCH, leaves the outputs unspecified and still orders `stream`
+ * after the enqueued work.
+ */
+int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
+                int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                int dtype, int chunks, fa_stream_t stream);
+
+/*
  * fa_softmax_rows -- numerically stable softmax of every row of x ("Guia Prático de
  * Programação de GPU com Tiles", section 4): y[r, :] = exp(x[r, :] - max) / sum exp(x[r, :] - max).
  *   x, y  [rows, cols] row-major device arrays, float32 (dtype 0) or bf16 (dtype 1)

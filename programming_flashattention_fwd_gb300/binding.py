@@ -46,6 +46,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.fa_fwd_select.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_int]
     lib.fa_fwd_debug.restype = ctypes.c_int
     lib.fa_fwd_debug.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
+    lib.fa_fwd_host.restype = ctypes.c_int
+    lib.fa_fwd_host.argtypes = ([ctypes.c_void_p] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
+                                                                                ctypes.c_int, ctypes.c_void_p])
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_strerror.argtypes = [ctypes.c_int]
     lib.fa_device_status.restype = ctypes.c_int
@@ -151,6 +154,29 @@ def fa_fwd_select(q, k, v, o, lse, causal, scale: float, kernel: int = 0, stream
     with 128-key steps, 2 one query tile per CTA with 64-key steps); bf16 or fp16."""
     _call("fa_fwd_select", q, k, v, o, lse, causal, scale, stream,
           extra=(int(q.dtype == torch.float16), int(kernel)))
+
+
+def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, causal, scale: float,
+                chunks: int = 0, stream=None) -> None:
+    """The forward on host (CPU, ideally pinned) tensors q_h, k_h, v_h into host o_h, lse_h,
+    staged through the caller's device buffers q_d .. lse_d of the same shapes; copies in,
+    kernels and copies back overlap chunk by chunk.  Asynchronous on `stream`."""
+    _check_tensors(q_d, k_d, v_d, o_d, lse_d)
+    for name, h, d in (("q_h", q_h, q_d), ("k_h", k_h, k_d), ("v_h", v_h, v_d), ("o_h", o_h, o_d),
+                       ("lse_h", lse_h, lse_d)):
+        if not isinstance(h, torch.Tensor) or h.is_cuda or not h.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+        if h.shape != d.shape or h.dtype != d.dtype:
+            raise ValueError(f"{name} must match its device buffer's shape and dtype")
+    B, Hq, Sq, D = q_d.shape
+    Hkv, Sk = k_d.shape[1], k_d.shape[2]
+    st = load_library().fa_fwd_host(
+        q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
+        q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(), lse_d.data_ptr(),
+        B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_d.dtype == torch.float16), int(chunks),
+        _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, fa_strerror(st))
 
 
 def attention(q, k, v, causal=False, scale: Optional[float] = None, stream=None,

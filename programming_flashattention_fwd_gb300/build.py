@@ -2,7 +2,7 @@
 
     python -m programming_flashattention_fwd_gb300.build [--verbose] [--force]
 
-The two translation units (kernel, host API) compile in parallel; the result lands next to
+The translation units (kernels, host API, host pipeline) compile in parallel; the result lands next to
 this file.  A rebuild is skipped when the library is newer than every source.
 """
 from __future__ import annotations
@@ -33,7 +33,8 @@ def nvcc() -> str:
 
 
 def sources():
-    return [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "fa_fwd1_sm103.cu", "gemm_sm103.cu", "softmax_sm103.cu", "fa_api.cpp")]
+    return [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "fa_fwd1_sm103.cu", "gemm_sm103.cu", "softmax_sm103.cu", "fa_api.cpp",
+                                                  "host_pipeline.cpp")]
 
 
 def _stale(path: str) -> bool:
@@ -67,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=5) as ex:
+    with ThreadPoolExecutor(max_workers=6) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = out + f".tmp{tag}"
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp, "-cudart", "static"]

@@ -58,15 +58,30 @@ bool encode(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, int 
     return r == CUDA_SUCCESS;
 }
 
-int check_device();
+} // namespace
 
-// kernel: 0 = automatic (two-tile for D <= 128, one-tile for D = 256), 1 = two query tiles per
-// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 128 / 256).
-int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
-        int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject,
-        int kernel = 0)
+namespace fa {
+
+// Device checks shared by every entry point (current device must be sm_103).
+int check_device()
 {
-    // ---- argument checks: no CUDA call before these pass
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
+    int st = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_NO_DEVICE;
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        g_arch_ok[dev].store(st, std::memory_order_relaxed);
+    }
+    return st == 1 ? FA_OK : FA_ERR_ARCH;
+}
+
+int check_fwd_args(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int Hq,
+                   int Hkv, int Sq, int Sk, int D, int causal, float scale, int kernel)
+{
     if (B < 0 || Sq < 0 || Sk < 0) return FA_ERR_BAD_DIM;
     if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_HEADS;
     if (kernel < 0 || kernel > 2) return FA_ERR_ARG;
@@ -78,9 +93,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     if (B == 0 || Sq == 0) return FA_OK;
     if (Sk == 0) return FA_ERR_BAD_DIM;
     const long long BHq = (long long)B * Hq, BHkv = (long long)B * Hkv;
-    const int key_tile = kernel == 2 ? 64 : fa::kBN;
-    const long long Tq = (Sq + fa::kBM - 1) / fa::kBM, Tk = (Sk + key_tile - 1) / key_tile;
-    const long long NP = (Tq + 1) / 2;
+    const long long Tq = (Sq + kBM - 1) / kBM;
     if (BHq * Tq > 0x7fffffffLL || BHq > 0x7fffffffLL) return FA_ERR_BAD_DIM;
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
@@ -90,10 +103,33 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
         ranges_overlap(lse, nl, q, nq) || ranges_overlap(lse, nl, k, nkv) || ranges_overlap(lse, nl, v, nkv) ||
         ranges_overlap(lse, nl, o, nq))
         return FA_ERR_ALIAS;
+    return FA_OK;
+}
+
+} // namespace fa
+
+namespace {
+
+// kernel: 0 = automatic (two-tile for D <= 128, one-tile for D = 256), 1 = two query tiles per
+// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 128 / 256).
+int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
+        int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject,
+        int kernel = 0)
+{
+    // ---- argument checks: no CUDA call before these pass
+    {
+        const int st = fa::check_fwd_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, kernel);
+        if (st != FA_OK || B == 0 || Sq == 0) return st;
+    }
+    if (kernel == 0) kernel = (D == 256) ? 2 : 1;
+    const long long BHq = (long long)B * Hq, BHkv = (long long)B * Hkv;
+    const int key_tile = kernel == 2 ? 64 : fa::kBN;
+    const long long Tq = (Sq + fa::kBM - 1) / fa::kBM, Tk = (Sk + key_tile - 1) / key_tile;
+    const long long NP = (Tq + 1) / 2;
 
     // ---- device
     {
-        const int st = check_device();
+        const int st = fa::check_device();
         if (st != FA_OK) return st;
     }
 
@@ -147,22 +183,6 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *base, bool bf16, l
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Device checks shared by every entry point (current device must be sm_103).
-int check_device()
-{
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
-    int st = g_arch_ok[dev].load(std::memory_order_relaxed);
-    if (st == 0) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return FA_ERR_NO_DEVICE;
-        st = (major == 10 && minor == 3) ? 1 : 2;
-        g_arch_ok[dev].store(st, std::memory_order_relaxed);
-    }
-    return st == 1 ? FA_OK : FA_ERR_ARCH;
-}
 
 } // namespace
 
@@ -185,7 +205,7 @@ int fa_gemm(const void *a, const void *b, void *c, const float *bias, int M, int
     if (ranges_overlap(c, nc, a, na) || ranges_overlap(c, nc, b, nb) ||
         (bias && ranges_overlap(c, nc, bias, (size_t)N * 4)))
         return FA_ERR_ALIAS;
-    int st = check_device();
+    int st = fa::check_device();
     if (st != FA_OK) return st;
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return FA_ERR_TENSORMAP;
@@ -219,7 +239,7 @@ int fa_softmax_rows(const void *x, void *y, int rows, int cols, int dtype, fa_st
     if (!aligned(x, al) || !aligned(y, al)) return FA_ERR_ALIGN;
     const size_t n = (size_t)rows * cols * (dtype == 0 ? 4 : 2);
     if (x != y && ranges_overlap(x, n, y, n)) return FA_ERR_ALIAS;   // in place is fine, partial overlap is not
-    int st = check_device();
+    int st = fa::check_device();
     if (st != FA_OK) return st;
     cudaError_t e = fa::launch_softmax_rows(dtype == 1, x, y, rows, cols, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;

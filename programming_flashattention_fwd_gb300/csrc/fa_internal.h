@@ -32,6 +32,13 @@ struct Maps {
     CUtensorMap q, k, v;
 };
 
+// Checks shared by the entry points, made before any CUDA call: the argument checks of
+// fa_fwd (returns FA_OK for a valid or empty problem, else the fa_status_t code), and
+// "the current device is an sm_103 part" (cached per device).
+int check_fwd_args(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int Hq,
+                   int Hkv, int Sq, int Sk, int D, int causal, float scale, int kernel);
+int check_device();
+
 // Launches the forward kernel for (D, dtype, causal).  Returns the cudaGetLastError() of the launch.
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const Maps &maps, const Params &p, cudaStream_t stream);
 

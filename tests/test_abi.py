@@ -165,3 +165,37 @@ def test_select_valid_pairs_pass_validation(lib):
     # call stop at the overlap check instead, before any CUDA call
     for kernel, D in ((0, 64), (0, 128), (0, 256), (1, 64), (1, 128), (2, 128), (2, 256)):
         assert lib.fa_fwd_select(Q, K, V, O, O + 16, 1, 4, 2, 256, 256, D, 1, 0.1, None, 0, kernel) == 6
+
+
+# fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, sizes..., dtype, chunks, stream)
+QH, KH, VH, OH, LH = 0xA0000000, 0xB0000000, 0xC0000000, 0xD0000000, 0xE0000000
+
+
+def call_host(lib, dtype=0, chunks=0, **over):
+    a = dict(GOOD, qh=QH, kh=KH, vh=VH, oh=OH, lh=LH, q=Q, k=K, v=V, o=O, lse=L)
+    a.update(over)
+    return lib.fa_fwd_host(a["qh"], a["kh"], a["vh"], a["oh"], a["lh"], a["q"], a["k"], a["v"], a["o"], a["lse"],
+                           a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["D"], a["causal"], a["scale"], dtype,
+                           chunks, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), 15), (dict(dtype=-1), 15), (dict(chunks=-1), 15), (dict(chunks=65), 15),
+    (dict(D=96), 4), (dict(Hq=3), 3), (dict(causal=3), 13), (dict(scale=math.inf), 7), (dict(Sk=0), 2),
+    (dict(qh=None), 1), (dict(lh=None), 1), (dict(o=None), 1),
+    (dict(q=Q + 8), 5), (dict(lse=L + 2), 5),
+    # written ranges must be disjoint from every other range
+    (dict(oh=QH + 64), 6), (dict(lh=OH + 4), 6), (dict(oh=Q), 6), (dict(qh=K + 16), 6), (dict(lh=KH), 6),
+    (dict(o=L), 6), (dict(k=V), 6),
+])
+def test_host_entry_point_invalid_arguments(lib, kw, code):
+    assert call_host(lib, **kw) == code
+
+
+def test_host_entry_point_empty_and_shared_inputs(lib):
+    # empty problems are no-ops before any pointer is looked at
+    assert call_host(lib, B=0, qh=None, kh=None, vh=None, oh=None, lh=None) == 0
+    assert call_host(lib, Sq=0) == 0
+    # host inputs may share memory (they are only read): the call then gets as far as the
+    # overlap checks of the written ranges, here a clash of lse_h with o_h
+    assert call_host(lib, kh=QH, vh=QH, lh=OH) == 6
