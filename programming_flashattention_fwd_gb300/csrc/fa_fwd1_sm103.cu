@@ -211,17 +211,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         auto issue_s = [&](uint32_t dS, uint32_t sQt, uint32_t sK) {
             const uint32_t qlo = sdesc_lo(sQt, 16), klo = sdesc_lo(sK, 16);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss_elect(dS, qlo + (uint32_t)(((kk >> 2) * C::QPANEL + (kk & 3) * 32) >> 4),
-                             klo + (uint32_t)(((kk >> 2) * C::KVPANEL + (kk & 3) * 32) >> 4), HI, idS, kk > 0);
+            for (int pn = 0; pn < D / 64; ++pn)   // 4 K-steps per 64-column panel
+                mma_ss_kk4_elect(dS, qlo + (uint32_t)((pn * C::QPANEL) >> 4), klo + (uint32_t)((pn * C::KVPANEL) >> 4),
+                                 HI, idS, pn > 0);
         };
         // O += P V over 64 keys: A = P from TMEM, B = V (MN-major, 64-column panels 8 KB apart)
         auto issue_pv = [&](uint32_t tP, uint32_t sV, bool first) {
             const uint32_t vlo = sdesc_lo(sV, C::KVPANEL);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ts_elect(tmem + C::COL_O, tP + kk * 8, vlo + (uint32_t)((kk * 2048) >> 4), HI, idPV,
-                             (first && kk == 0) ? 0u : 1u);
+            static_assert(BN == 64, "one four-step group covers the 64 keys");
+            mma_ts_mn4_elect(tmem + C::COL_O, tP, vlo, HI, idPV, first ? 0u : 1u);
         };
         auto tS = [&](uint32_t gs) { return tmem + ((gs & 1) ? C::COL_S1 : C::COL_S0); };
         int use = 0, tau = 0;

@@ -273,22 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s = [&](uint32_t dS, uint32_t sQt, uint32_t sK) {
                 const uint32_t qlo = sdesc_lo(sQt, 16), klo = sdesc_lo(sK, 16);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * C::PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss_elect(dS, qlo + off, klo + off, HI, idS, kk > 0);
+                for (int pn = 0; pn < C::PANELS; ++pn) {   // 4 K-steps per 64-column panel
+                    const uint32_t off = (uint32_t)(pn * C::PANEL) >> 4;
+                    mma_ss_kk4_elect(dS, qlo + off, klo + off, HI, idS, pn > 0);
                 }
             };
             // O += P V for keys [64h, 64h+64): A = P from TMEM (16-bit pairs per column),
             // B = V tile, MN-major (D contiguous per key row): 8-key groups 1024 bytes apart,
-            // 64-column panels C::PANEL bytes apart; 16 keys per instruction.
+            // 64-column panels C::PANEL bytes apart; 16 keys per K-step.
             auto issue_pv_half = [&](uint32_t dO, uint32_t tP, uint32_t sV, int h, bool first) {
                 const uint32_t vlo = sdesc_lo(sV, C::PANEL);
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int kk = 4 * h + k4;
-                    mma_ts_elect(dO, tP + kk * 8, vlo + (uint32_t)((kk * 2048) >> 4), HI, idPV,
-                                 (first && kk == 0) ? 0u : 1u);
-                }
+                mma_ts_mn4_elect(dO, tP + 32 * h, vlo + (uint32_t)((4 * h * 2048) >> 4), HI, idPV,
+                                 (first && h == 0) ? 0u : 1u);
             };
 
             int use = 0;               // ring uses consumed (K_j = use, V_j = use + 1 within a step)

@@ -165,10 +165,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t sA = sb + s * STAGE_BYTES, sB = sA + A_BYTES;
                 const uint32_t alo = sdesc_lo(sA, 16), blo = sdesc_lo(sB, B_PANEL);
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_ss_elect(d, alo + (uint32_t)((kk * 32) >> 4), blo + (uint32_t)((kk * 2048) >> 4), HI, idesc,
-                                  (kb > 0 || kk > 0) ? 1u : 0u);
+                static_assert(BK == 64, "one four-step group covers the K block");
+                mma_ss_kmn4_elect(d, alo, blo, HI, idesc, kb > 0 ? 1u : 0u);
                 tc_commit_elect(bar_empty(s));
             }
             if (!ok) break;

@@ -297,29 +297,55 @@ __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, 
 // picks one lane, which alone issues the instruction.  Descriptors are passed as their two
 // 32-bit halves: the low word carries the start address and leading offset, the high word
 // the stride offset, version and swizzle mode.
-__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
-                                             uint32_t idesc, uint32_t accumulate)
+//
+// Four K-steps (K = 64) of one MMA behind a single elect.sync, the per-step descriptor offsets
+// applied inside the block: fewer instructions per MMA for the issuing warp.  Offsets are in
+// 16-byte units: a K-major operand advances 32 bytes (2) per K-step inside its 128-byte swizzle
+// atom; an MN-major operand advances one 16-row group of 128-byte rows, 2048 bytes (128).  The
+// first step accumulates iff `accumulate`, the other three always do.
+#define FA_MMA_SS_STEP(AOFF, BOFF)                                                                 \
+    "add.u32 al, %1, " #AOFF ";\n\tadd.u32 bl, %2, " #BOFF ";\n\t"                                 \
+    "mov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"                                          \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+#define FA_MMA_SS_HEAD                                                                             \
+    "{\n\t.reg .b32 al, bl;\n\t.reg .b64 a, b;\n\t.reg .pred p, e, t;\n\t"                        \
+    "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"             \
+    "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"                                          \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t"
+// A and B both K-major (S = Q K^T).
+__device__ __forceinline__ void mma_ss_kk4_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                 uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile("{\n\t.reg .b64 a, b;\n\t.reg .pred p, e;\n\t"
-                 "mov.b64 a, {%1, %3};\n\t"
-                 "mov.b64 b, {%2, %3};\n\t"
-                 "setp.ne.b32 p, %5, 0;\n\t"
-                 "elect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+    asm volatile(FA_MMA_SS_HEAD FA_MMA_SS_STEP(2, 2) FA_MMA_SS_STEP(4, 4) FA_MMA_SS_STEP(6, 6) "}" ::"r"(d_tmem),
                  "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
-                                             uint32_t idesc, uint32_t accumulate)
+// A K-major, B MN-major (C = A B with B row-major).
+__device__ __forceinline__ void mma_ss_kmn4_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                  uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile("{\n\t.reg .b64 b;\n\t.reg .pred p, e;\n\t"
-                 "mov.b64 b, {%2, %3};\n\t"
-                 "setp.ne.b32 p, %5, 0;\n\t"
-                 "elect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+    asm volatile(FA_MMA_SS_HEAD FA_MMA_SS_STEP(2, 128) FA_MMA_SS_STEP(4, 256) FA_MMA_SS_STEP(6, 384) "}" ::"r"(d_tmem),
+                 "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
+#undef FA_MMA_SS_STEP
+#undef FA_MMA_SS_HEAD
+#define FA_MMA_TS_STEP(TOFF, BOFF)                                                                 \
+    "add.u32 ta, %1, " #TOFF ";\n\tadd.u32 bl, %2, " #BOFF ";\n\tmov.b64 b, {bl, %3};\n\t"          \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+// A from tensor memory (16-bit pairs: 8 columns per K-step), B MN-major (O += P V).
+__device__ __forceinline__ void mma_ts_mn4_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                 uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .b32 ta, bl;\n\t.reg .b64 b;\n\t.reg .pred p, e, t;\n\t"
+                 "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "mov.b64 b, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t"
+                 FA_MMA_TS_STEP(8, 128) FA_MMA_TS_STEP(16, 256) FA_MMA_TS_STEP(24, 384)
+                 "}" ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+#undef FA_MMA_TS_STEP
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar)
 {
     asm volatile("{\n\t.reg .pred e;\n\t"
