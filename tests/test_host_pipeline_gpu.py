@@ -61,6 +61,7 @@ CASES = [
     ("one_chunk", 1, 4, 2, 64, 64, 128, "bf16", 1, 1),
     ("chunks_above_groups", 1, 4, 2, 64, 64, 128, "bf16", 1, 64),
     ("one_head_per_chunk", 2, 6, 3, 200, 333, 64, "fp16", 0, 6),
+    ("auto_cross", 3, 8, 4, 160, 200, 64, "bf16", 1, 0),   # automatic: 4 runs of 3 KV heads, one crossing a batch
 ]
 
 
