@@ -245,7 +245,9 @@ def time_oracle(w, q, k, v, target_s: float, seed: int):
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(rows)} seeded query rows of {w.name} (all heads/batches), "
                       f"float64 C oracle with OpenMP, {dt:.1f} s",
-            "rows": int(len(rows)), "seconds": round(dt, 3)}
+            "rows": int(len(rows)), "seconds": round(dt, 3), "rows_per_s": round(len(rows) / dt, 1),
+            "float64_gflops": round(flops / dt / 1e9, 2),
+            "full_workload_s_extrapolated": round(w.flops() / (flops / dt), 2)}
 
 
 def run_reference(args, w, world, rank):
