@@ -140,3 +140,21 @@ def test_host_entry_binding_rejects_bad_tensors(fa):
         fa.fa_fwd_host(*hb[:3], hb[3][:, :1].contiguous(), hb[4], *db, 0, 0.125)   # wrong shape
     with pytest.raises(fa.FaError):
         fa.fa_fwd_host(*hb, *db, 0, 0.125, chunks=100)
+
+
+def test_host_entry_two_calls_in_flight(fa):
+    """Calls on two caller streams, each with its own staging buffers and host outputs, enqueued
+    alternately without synchronising in between (the benchmark's end-to-end pattern): the
+    shared internal streams and events must keep every call's copies and kernels ordered."""
+    w = Workload("inflight", 2, 8, 2, 700, 900, 128, "bf16", 2, seed=31)
+    q, k, v = make_qkv(w)
+    o_ref, l_ref = reference_device_run(fa, w, q, k, v)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    hbs = [host_buffers(q, k, v, True) for _ in range(2)]
+    dbs = [device_buffers(q, k, v) for _ in range(2)]
+    for i in range(6):
+        fa.fa_fwd_host(*hbs[i % 2], *dbs[i % 2], w.causal, w.softmax_scale, chunks=3, stream=streams[i % 2])
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == (0, 0)
+    for hb in hbs:
+        assert torch.equal(hb[3], o_ref) and torch.equal(hb[4], l_ref)
