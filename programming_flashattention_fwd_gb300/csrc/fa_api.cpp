@@ -164,6 +164,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.coff = causal == 2 ? Sk - Sq : 0;
     p.timeout_ns = timeout_ns;
     p.inject = inject;
+    p.o_al32 = aligned(o, 32) ? 1u : 0u;   // rows are 2*D bytes, so every row then starts on 32 bytes
 
     cudaError_t e = kernel == 2 ? fa::launch_fwd1(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream))
                                 : fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));

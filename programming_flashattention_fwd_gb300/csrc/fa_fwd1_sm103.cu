@@ -419,9 +419,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     pk[e] = pack2<BF16>(lo, hi);
                 }
                 if (row < p.Sq) {
+                    if (p.o_al32) {   // full 32-byte sectors: half the store instructions, no partial sectors
+                        st_global_v8(orow + c * 2, pk);
+                        st_global_v8(orow + c * 2 + 32, pk + 8);
+                    } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        st_global_v4(orow + c * 2 + q4 * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            st_global_v4(orow + c * 2 + q4 * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
+                                         pk[4 * q4 + 3]);
+                    }
                 }
             }
             if (row < p.Sq) {

@@ -25,6 +25,7 @@ struct Params {
     int coff;           // causal offset: key j allowed for query i iff j <= i + coff (0 top-left, Sk - Sq bottom-right)
     uint64_t timeout_ns;// watchdog limit of each bounded wait
     uint32_t inject;    // fault-injection mask (0 in normal use)
+    uint32_t o_al32;    // o is 32-byte aligned: output rows are written in full 32-byte sectors
 };
 
 // The TMA descriptors: q, k, v as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.

@@ -287,6 +287,13 @@ __device__ __forceinline__ void regs_inc()
 }
 
 // 16-byte global store
+// One full 32-byte sector per lane; ptr must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t *v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
 __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
