@@ -67,15 +67,40 @@ KERNEL_SOURCES = {
 }
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments and without blank lines (string and
+    character literals are kept as they are), so that editing a comment does not count as a
+    change of the code."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """sha256 of the sources `kernel` is built from: ties an ncu traffic figure to the code it
-    measured (a change to another kernel leaves it valid)."""
+    """sha256 of the sources `kernel` is built from, comments removed: ties an ncu traffic
+    figure to the code it measured (a change to another kernel leaves it valid)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "programming_flashattention_fwd_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[kernel] + COMMON_SOURCES):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

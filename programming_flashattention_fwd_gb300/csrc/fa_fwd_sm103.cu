@@ -15,7 +15,8 @@
 // pipe runs the other tile's MMAs.
 //
 //   warp 0        TMA producer of K_j, V_j into a ring of shared-memory slots
-//   warp 1        TMEM allocator + MMA issuer (one thread): S_x = Q_x K_j^T, O_x += P_x V_j
+//   warp 1        TMEM allocator + MMA issuer: S_x = Q_x K_j^T, O_x += P_x V_j (the whole warp in
+//                 uniform control flow; one elected lane issues each group of four K-steps)
 //   warp 2        TMA producer of query tiles into three rotating Q buffers
 //   warp 3        idle
 //   warps 4-7     softmax + correction + epilogue of tile a of every unit (one thread per row)
@@ -31,7 +32,7 @@
 // unnormalised P stays <= 256, well inside bf16/fp16 range; O and l always share the same
 // stale max, so the result is unchanged); K/V tails and the causal diagonal are masked only
 // on the tiles that need it; fully masked causal tiles are skipped; the log-sum-exp is
-// written out.
+// written out; output rows go out in full 32-byte sectors when o is 32-byte aligned.
 //
 // Every wait is bounded (watchdog): on expiry the kernel records a status word, raises a
 // CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM and returns.
