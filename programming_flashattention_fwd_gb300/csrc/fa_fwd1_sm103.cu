@@ -154,11 +154,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ K/V producer (consumption order)
         if (lane == 0) {
             int use = 0;
+            int skip = -1;   // fault injection (inject bit 0): the first V tile is never loaded
             bool ok = true;
             auto load = [&](const CUtensorMap *m, int j, int zkv) {
                 const int s = use % C::NS;
                 if (!bounded_wait(bar_empty(s), ((use / C::NS) & 1) ^ 1, abort_flag, tmo, S_EMPTY, status))
                     return false;
+                if ((p.inject & 1u) && m == &tmV && skip < 0) {
+                    skip = use++;
+                    return true;
+                }
                 mbar_arrive_expect_tx(bar_full(s), C::KVTILE);
 #pragma unroll
                 for (int pn = 0; pn < C::PANELS; ++pn)
@@ -176,7 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             for (int x = max(0, use - C::NS); x < use; ++x)
-                bounded_wait(bar_full(x % C::NS), (x / C::NS) & 1, abort_flag, tmo, S_DRAIN, status, false);
+                if (x != skip)
+                    bounded_wait(bar_full(x % C::NS), (x / C::NS) & 1, abort_flag, tmo, S_DRAIN, status, false);
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ Q producer

@@ -248,10 +248,11 @@ def test_attention_convenience_matches(fa):
     assert torch.equal(o, o2) and torch.equal(lse, l2)
 
 
-def test_watchdog_reports_and_recovers(fa, orc):
+@pytest.mark.parametrize("D", [64, 256])   # the two-tile kernel (D 64) and the one-tile kernel (D 256)
+def test_watchdog_reports_and_recovers(fa, orc, D):
     """An injected missing V load makes the bounded waits expire: the call reports
     FA_ERR_DEVICE_TIMEOUT through fa_device_status and the context stays usable."""
-    w = Workload("wd", 1, 2, 2, 256, 256, 64, "bf16", False, 5)
+    w = Workload("wd", 1, 2, 2, 256, 256, D, "bf16", False, 5)
     q, k, v = (t.cuda() for t in make_qkv(w))
     o = torch.zeros_like(q)
     lse = torch.zeros(q.shape[:3], dtype=torch.float32, device="cuda")
