@@ -522,16 +522,18 @@ def run_op(args, world, rank, local):
         d2h = c.numel() * 2
     else:
         R, C = args.rows, args.cols
-        x_h = torch.randn((R, C), generator=g) * 4.0
+        sdt = torch.bfloat16 if args.softmax_dtype == "bf16" else torch.float32
+        esz = 2 if args.softmax_dtype == "bf16" else 4
+        x_h = (torch.randn((R, C), generator=g) * 4.0).to(sdt)
         x = x_h.to(dev)
         y = torch.empty_like(x)
         call = lambda: binding.softmax_rows(x, y)
-        work = 2.0 * R * C * 4
-        name = f"softmax_fp32_{R}x{C}"
+        work = 2.0 * R * C * esz
+        name = f"softmax_{args.softmax_dtype}_{R}x{C}"
         metric, unit, bound = "row softmax GB/s (bytes read + written)", "GB/s", "hbm"
         scale = 1e9
-        cfg = {"workload": name, "rows": R, "cols": C, "dtype": "fp32"}
-        h2d, d2h = x_h.numel() * 4, x_h.numel() * 4
+        cfg = {"workload": name, "rows": R, "cols": C, "dtype": args.softmax_dtype}
+        h2d, d2h = x_h.numel() * esz, x_h.numel() * esz
 
     for _ in range(args.warmup):
         call()
@@ -614,7 +616,7 @@ def run_op(args, world, rank, local):
     else:
         ids = np.random.default_rng(5).integers(0, R, 512)
         orc.softmax_rows(x_h, ids)
-        cpu_work, sample = 2.0 * len(ids) * C * 4, f"{len(ids)} seeded rows of {name}, float64 C oracle"
+        cpu_work, sample = 2.0 * len(ids) * C * esz, f"{len(ids)} seeded rows of {name}, float64 C oracle"
     dt = time.perf_counter() - t0
     line = {
         "metric": metric, "value": work * world / t_step / scale, "unit": unit, "n_gpus": world,
@@ -659,6 +661,7 @@ def main():
     ap.add_argument("--K", type=int, default=8192)
     ap.add_argument("--rows", type=int, default=65536)
     ap.add_argument("--cols", type=int, default=4096)
+    ap.add_argument("--softmax-dtype", default="fp32", choices=["fp32", "bf16"])
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -303,7 +303,9 @@ int fa_device_status(fa_stream_t stream, uint32_t *detail)
     uint32_t w1 = 0;
     if (fa::read_and_clear_gemm_status(&wg) != cudaSuccess) return FA_ERR_NO_DEVICE;
     if (fa::read_and_clear_fa1_status(&w1) != cudaSuccess) return FA_ERR_NO_DEVICE;
-    if (!(w & 1u)) w = (w1 & 1u) ? w1 : wg;   // first expiry wins, attention kernels checked first
+    uint32_t ws = 0;
+    if (fa::read_and_clear_softmax_status(&ws) != cudaSuccess) return FA_ERR_NO_DEVICE;
+    if (!(w & 1u)) w = (w1 & 1u) ? w1 : ((wg & 1u) ? wg : ws);   // attention kernels checked first
     if (detail) *detail = w;
     return (w & 1u) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }

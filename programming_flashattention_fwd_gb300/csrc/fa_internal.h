@@ -69,5 +69,6 @@ cudaError_t read_and_clear_gemm_status(uint32_t *word);
 // ---------------------------------------------------------------- row softmax
 // x, y: [rows, cols] row-major, fp32 or bf16 (same type); one launch, any cols >= 1.
 cudaError_t launch_softmax_rows(bool bf16, const void *x, void *y, int rows, int cols, cudaStream_t stream);
+cudaError_t read_and_clear_softmax_status(uint32_t *word);
 
 } // namespace fa

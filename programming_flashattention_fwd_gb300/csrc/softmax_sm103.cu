@@ -2,10 +2,14 @@
 //
 // "Guia Prático de Programação de GPU com Tiles", section 4 (row softmax, one row per
 // program): subtract the row maximum, exponentiate, sum, divide; columns past the row's end
-// do not take part.  Here a row is handled by one warp (short rows) or one 256-thread CTA
-// (rows up to 8192 fp32 / 16384 bf16 values), held in registers between one coalesced read
-// and one write -- an HBM-bound kernel touches each byte once.  Longer rows take two passes
-// (an online max/sum pass, then a normalising pass over the same row, mostly from L2).
+// do not take part.  The kernel is HBM-bound, so each byte is read once and written once:
+//  - rows up to 8192 values live in registers, a group of G = 32 .. 256 threads per row with
+//    at most 32 values per thread, sized to the row so that short rows keep many rows (and
+//    loads) in flight per SM;
+//  - longer rows that fit shared memory are copied there whole by the bulk-copy engine, two
+//    row buffers per CTA so the next row streams in while this one is normalised;
+//  - rows beyond that take two passes (an online max/sum pass, then a normalising pass that
+//    re-reads the row).
 //
 // x and y are [rows, cols] row-major, both fp32 or both bf16; arithmetic is fp32, exp via
 // exp2 with the input pre-scaled by log2(e).
@@ -15,22 +19,32 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "watchdog.cuh"
 
 namespace fa {
+
+__device__ unsigned int g_softmax_status;   // watchdog word of the shared-memory path
+
 namespace sm {
 
 constexpr int THREADS = 256;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 template <bool BF16>
 struct IO;
 template <>
 struct IO<false> {   // fp32, vectors of 4
     static constexpr int VEC = 4;
+    static constexpr int ESZ = 4;
     __device__ static void load(const void *base, size_t i, float (&v)[4])
     {
         const float4 f = __ldg(reinterpret_cast<const float4 *>(base) + i);
         v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+    }
+    __device__ static void load_smem(uint32_t addr, float (&v)[4])
+    {
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
     }
     __device__ static float load1(const void *base, size_t i) { return __ldg(reinterpret_cast<const float *>(base) + i); }
     __device__ static void store(void *base, size_t i, const float (&v)[4])
@@ -43,15 +57,26 @@ struct IO<false> {   // fp32, vectors of 4
 template <>
 struct IO<true> {    // bf16, vectors of 8
     static constexpr int VEC = 8;
-    __device__ static void load(const void *base, size_t i, float (&v)[8])
+    static constexpr int ESZ = 2;
+    __device__ static void unpack(const uint32_t (&w)[4], float (&v)[8])
     {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(base) + i);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             v[2 * k] = __uint_as_float(w[k] << 16);
             v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
         }
+    }
+    __device__ static void load(const void *base, size_t i, float (&v)[8])
+    {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(base) + i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        unpack(w, v);
+    }
+    __device__ static void load_smem(uint32_t addr, float (&v)[8])
+    {
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+        unpack(w, v);
     }
     __device__ static float load1(const void *base, size_t i)
     {
@@ -68,7 +93,9 @@ struct IO<true> {    // bf16, vectors of 8
     }
 };
 
-// Reduction over a group of G threads (G = 32: one warp; G = 256: the CTA through shared memory).
+// Reduction over the G consecutive threads of a group (G = 32: one warp, by shuffles; G = 64 ..
+// 256: the group's warps combine through shared memory).  Every thread of the CTA calls it the
+// same number of times.
 template <int G, bool MAX>
 __device__ __forceinline__ float group_reduce(float v, float *scratch)
 {
@@ -77,15 +104,20 @@ __device__ __forceinline__ float group_reduce(float v, float *scratch)
         const float w = __shfl_xor_sync(0xffffffffu, v, o);
         v = MAX ? fmaxf(v, w) : v + w;
     }
-    if (G == 32) return v;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();                    // scratch free from the previous reduction
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    float r = scratch[0];
+    if constexpr (G == 32) {
+        return v;
+    } else {
+        constexpr int NW = G / 32;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        __syncthreads();                    // scratch free from the previous reduction
+        if (lane == 0) scratch[warp] = v;
+        __syncthreads();
+        const int w0 = (warp / NW) * NW;
+        float r = scratch[w0];
 #pragma unroll
-    for (int w = 1; w < G / 32; ++w) r = MAX ? fmaxf(r, scratch[w]) : r + scratch[w];
-    return r;
+        for (int w = 1; w < NW; ++w) r = MAX ? fmaxf(r, scratch[w0 + w]) : r + scratch[w0 + w];
+        return r;
+    }
 }
 
 // Rows held in registers: a group of G threads per row, at most NV vectors per thread.
@@ -147,43 +179,190 @@ __global__ void __launch_bounds__(THREADS) softmax_regs_kernel(const void *x, vo
     }
 }
 
-// Any row length: pass 1 keeps a running (max, sum) per thread and merges them; pass 2
-// re-reads the row (from L2 for all but very long rows) and writes the normalised values.
-template <bool BF16>
-__global__ void __launch_bounds__(THREADS) softmax_twopass_kernel(const void *x, void *y, int rows, int cols)
+// Rows copied whole into shared memory by the bulk-copy engine: NBUF row buffers per CTA (the
+// next row streams in while this one is normalised).  Three passes over the shared copy (max,
+// sum of exponentials, normalised write); x is read from HBM exactly once.  Rows are 16-byte
+// aligned (cols a multiple of the vector width, x aligned).
+constexpr uint32_t kBulkChunk = 32768;   // bytes per bulk-copy instruction
+
+template <bool BF16, int NBUF>
+__global__ void __launch_bounds__(THREADS) softmax_smem_kernel(const void *x, void *y, int rows, int cols,
+                                                                uint32_t row_bytes)
 {
+    constexpr int W = IO<BF16>::VEC;
+    extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float scratch[THREADS / 32];
-    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
-        float m = -INFINITY, s = 0.f;   // running max and sum of exp(x - m)
-        for (int c = threadIdx.x; c < cols; c += THREADS) {
-            const float xv = IO<BF16>::load1(x, (size_t)r * cols + c);
-            if (xv > m) {
-                s = s * ex2_approx((m - xv) * kLog2e) + 1.f;
-                m = xv;
-            } else {
-                s += ex2_approx((xv - m) * kLog2e);
-            }
+    __shared__ __align__(8) uint64_t bars[NBUF];
+    __shared__ int abort_flag;
+    const uint32_t base = smem_u32(dsm);
+    const int nvec = cols / W;
+    const long long my_rows = rows > (int)blockIdx.x ? (rows - 1 - (long long)blockIdx.x) / gridDim.x + 1 : 0;
+    auto bar = [&](int b) { return smem_u32(&bars[b]); };
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < NBUF; ++b) mbar_init(bar(b), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // thread 0: copy the CTA's i-th row into buffer i % NBUF
+    auto issue = [&](long long i) {
+        const long long r = blockIdx.x + i * gridDim.x;
+        const int b = (int)(i % NBUF);
+        const uint32_t dst = base + (uint32_t)b * row_bytes;
+        const char *src = static_cast<const char *>(x) + (size_t)r * row_bytes;
+        mbar_arrive_expect_tx(bar(b), row_bytes);
+        for (uint32_t off = 0; off < row_bytes; off += kBulkChunk)
+            bulk_load(dst + off, src + off, min(kBulkChunk, row_bytes - off), bar(b));
+    };
+    if (threadIdx.x == 0)
+        for (long long i = 0; i < NBUF && i < my_rows; ++i) issue(i);
+    for (long long i = 0; i < my_rows; ++i) {
+        const long long r = blockIdx.x + i * gridDim.x;
+        const int b = (int)(i % NBUF);
+        if (!bounded_wait(bar(b), (uint32_t)((i / NBUF) & 1), &abort_flag, kTimeoutNs, 1, &g_softmax_status, false))
+            return;   // every thread waits on the same copy, so all of them give up together
+        const uint32_t rb = base + (uint32_t)b * row_bytes;
+        float mx = -INFINITY;
+        for (int vi = threadIdx.x; vi < nvec; vi += THREADS) {
+            float v[W];
+            IO<BF16>::load_smem(rb + (uint32_t)vi * 16u, v);
+#pragma unroll
+            for (int e = 0; e < W; ++e) mx = fmaxf(mx, v[e]);
         }
-        const float mr = group_reduce<THREADS, true>(m, scratch);
-        const float sr = group_reduce<THREADS, false>(m == -INFINITY ? 0.f : s * ex2_approx((m - mr) * kLog2e), scratch);
-        const float inv = 1.f / sr, mb = mr * kLog2e;
-        for (int c = threadIdx.x; c < cols; c += THREADS) {
-            const float xv = IO<BF16>::load1(x, (size_t)r * cols + c);
-            IO<BF16>::store1(y, (size_t)r * cols + c, ex2_approx(fmaf(xv, kLog2e, -mb)) * inv);
+        mx = group_reduce<THREADS, true>(mx, scratch);
+        const float mb = mx * kLog2e;
+        float sum = 0.f;
+        for (int vi = threadIdx.x; vi < nvec; vi += THREADS) {
+            float v[W];
+            IO<BF16>::load_smem(rb + (uint32_t)vi * 16u, v);
+#pragma unroll
+            for (int e = 0; e < W; ++e) sum += ex2_approx(fmaf(v[e], kLog2e, -mb));
+        }
+        sum = group_reduce<THREADS, false>(sum, scratch);
+        const float inv = 1.f / sum;
+        for (int vi = threadIdx.x; vi < nvec; vi += THREADS) {
+            float v[W];
+            IO<BF16>::load_smem(rb + (uint32_t)vi * 16u, v);
+#pragma unroll
+            for (int e = 0; e < W; ++e) v[e] = ex2_approx(fmaf(v[e], kLog2e, -mb)) * inv;
+            IO<BF16>::store(y, (size_t)r * nvec + vi, v);
+        }
+        __syncthreads();   // every thread has finished reading buffer b
+        if (threadIdx.x == 0 && i + NBUF < my_rows) {
+            fence_proxy_async_smem();
+            issue(i + NBUF);
         }
     }
 }
 
+// Any row length: pass 1 keeps a running (max, sum) per thread and merges them; pass 2
+// re-reads the row and writes the normalised values.  VECTOR: 16-byte vectors.
+template <bool BF16, bool VECTOR>
+__global__ void __launch_bounds__(THREADS) softmax_twopass_kernel(const void *x, void *y, int rows, int cols)
+{
+    constexpr int W = VECTOR ? IO<BF16>::VEC : 1;
+    __shared__ float scratch[THREADS / 32];
+    const int n = cols / W;
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        float m = -INFINITY, s = 0.f;   // running max and sum of exp(x - m)
+        for (int c = threadIdx.x; c < n; c += THREADS) {
+            float v[W];
+            if constexpr (VECTOR) {
+                IO<BF16>::load(x, (size_t)r * n + c, v);
+            } else {
+                v[0] = IO<BF16>::load1(x, (size_t)r * cols + c);
+            }
+            float vm = v[0];
+#pragma unroll
+            for (int e = 1; e < W; ++e) vm = fmaxf(vm, v[e]);
+            if (vm > m) {
+                s = (m == -INFINITY) ? 0.f : s * ex2_approx((m - vm) * kLog2e);
+                m = vm;
+            }
+            const float mb = m * kLog2e;
+#pragma unroll
+            for (int e = 0; e < W; ++e) s += ex2_approx(fmaf(v[e], kLog2e, -mb));
+        }
+        const float mr = group_reduce<THREADS, true>(m, scratch);
+        const float sr = group_reduce<THREADS, false>(m == -INFINITY ? 0.f : s * ex2_approx((m - mr) * kLog2e), scratch);
+        const float inv = 1.f / sr, mb = mr * kLog2e;
+        for (int c = threadIdx.x; c < n; c += THREADS) {
+            float v[W];
+            if constexpr (VECTOR) {
+                IO<BF16>::load(x, (size_t)r * n + c, v);
+#pragma unroll
+                for (int e = 0; e < W; ++e) v[e] = ex2_approx(fmaf(v[e], kLog2e, -mb)) * inv;
+                IO<BF16>::store(y, (size_t)r * n + c, v);
+            } else {
+                v[0] = IO<BF16>::load1(x, (size_t)r * cols + c);
+                IO<BF16>::store1(y, (size_t)r * cols + c, ex2_approx(fmaf(v[0], kLog2e, -mb)) * inv);
+            }
+        }
+    }
+}
+
+static cudaError_t sm_count(int *nsm)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev);
+}
+
+// Grid-stride launch over `units` (rows or row groups), at most eight CTAs per SM.
 template <typename K>
 static cudaError_t launch_grid(K kern, long long units, const void *x, void *y, int rows, int cols, cudaStream_t st)
 {
-    int dev = 0, nsm = 1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    int nsm = 1;
+    cudaError_t e = sm_count(&nsm);
     if (e != cudaSuccess) return e;
     const long long grid = units < (long long)nsm * 8 ? units : (long long)nsm * 8;
     kern<<<(int)(grid > 0 ? grid : 1), THREADS, 0, st>>>(x, y, rows, cols);
+    return cudaGetLastError();
+}
+
+// The register kernel with G threads per row and NV vectors per thread.  A thread holds at most
+// 32 values (NV * vector width): more registers per thread cost more in resident warps than
+// they gain (bf16 rows of 8192 values: 5051 GB/s with 8 vectors per thread, 6510 with 4).
+template <bool BF16, bool VECTOR>
+constexpr int kMaxNV = (VECTOR && BF16) ? 4 : 8;
+
+template <bool BF16, bool VECTOR>
+static cudaError_t launch_regs(long long n, const void *x, void *y, int rows, int cols, cudaStream_t st)
+{
+    constexpr int NVM = kMaxNV<BF16, VECTOR>;
+#define FA_SM_CASE(GG, NN)                                                                                   \
+    if (n <= (long long)(GG) * (NN))                                                                         \
+        return launch_grid(softmax_regs_kernel<BF16, GG, NN, VECTOR>, ((long long)rows + THREADS / (GG) - 1) / (THREADS / (GG)), \
+                           x, y, rows, cols, st);
+    FA_SM_CASE(32, 1) FA_SM_CASE(32, 2) FA_SM_CASE(32, 4)
+    if constexpr (NVM == 8) {
+        FA_SM_CASE(32, 8)
+    }
+    if constexpr (NVM == 8) {   // fp32: 4096 values as one 256-thread group (6740 GB/s) rather than two of 128 (6560)
+        FA_SM_CASE(64, 8) FA_SM_CASE(256, 8)
+    } else {
+        FA_SM_CASE(64, NVM) FA_SM_CASE(128, NVM) FA_SM_CASE(256, NVM)
+    }
+#undef FA_SM_CASE
+    return cudaErrorInvalidValue;
+}
+
+constexpr uint32_t kSmemLimit = 227 * 1024 - 1024;  // dynamic shared memory for row buffers
+
+template <bool BF16, int NBUF>
+static cudaError_t launch_smem(const void *x, void *y, int rows, int cols, uint32_t row_bytes, cudaStream_t st)
+{
+    auto kern = softmax_smem_kernel<BF16, NBUF>;
+    const uint32_t smem = NBUF * row_bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int nsm = 1;
+    if ((e = sm_count(&nsm)) != cudaSuccess) return e;
+    const int per_sm = (int)(kSmemLimit / smem) > 0 ? (int)(kSmemLimit / smem) : 1;
+    const long long cap = (long long)nsm * per_sm;
+    const int grid = (int)(rows < cap ? rows : cap);
+    kern<<<grid, THREADS, smem, st>>>(x, y, rows, cols, row_bytes);
     return cudaGetLastError();
 }
 
@@ -192,15 +371,18 @@ static cudaError_t launch_typed(const void *x, void *y, int rows, int cols, cuda
 {
     constexpr int W = IO<BF16>::VEC;
     const bool vec = (cols % W == 0) && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % 16 == 0);
-    constexpr int NV = 8;
+    const long long n = vec ? cols / W : cols;
+    if (vec && n <= (long long)THREADS * kMaxNV<BF16, true>) return launch_regs<BF16, true>(n, x, y, rows, cols, st);
+    if (!vec && n <= (long long)THREADS * kMaxNV<BF16, false>) return launch_regs<BF16, false>(n, x, y, rows, cols, st);
     if (vec) {
-        if (cols <= 32 * NV * W) return launch_grid(softmax_regs_kernel<BF16, 32, NV, true>, ((long long)rows + 7) / 8, x, y, rows, cols, st);
-        if (cols <= THREADS * NV * W) return launch_grid(softmax_regs_kernel<BF16, THREADS, NV, true>, rows, x, y, rows, cols, st);
-    } else {
-        if (cols <= 32 * NV) return launch_grid(softmax_regs_kernel<BF16, 32, NV, false>, ((long long)rows + 7) / 8, x, y, rows, cols, st);
-        if (cols <= THREADS * NV) return launch_grid(softmax_regs_kernel<BF16, THREADS, NV, false>, rows, x, y, rows, cols, st);
+        const uint64_t row_bytes = (uint64_t)cols * IO<BF16>::ESZ;
+        if (2 * row_bytes <= kSmemLimit) return launch_smem<BF16, 2>(x, y, rows, cols, (uint32_t)row_bytes, st);
+        if (row_bytes <= kSmemLimit) return launch_smem<BF16, 1>(x, y, rows, cols, (uint32_t)row_bytes, st);
+        // (one CTA per SM would keep the re-read in L2 but holds too few loads in flight: 2109
+        // against 4338 GB/s for fp32 rows of 65536 values)
+        return launch_grid(softmax_twopass_kernel<BF16, true>, rows, x, y, rows, cols, st);
     }
-    return launch_grid(softmax_twopass_kernel<BF16>, rows, x, y, rows, cols, st);
+    return launch_grid(softmax_twopass_kernel<BF16, false>, rows, x, y, rows, cols, st);
 }
 
 } // namespace sm
@@ -208,6 +390,17 @@ static cudaError_t launch_typed(const void *x, void *y, int rows, int cols, cuda
 cudaError_t launch_softmax_rows(bool bf16, const void *x, void *y, int rows, int cols, cudaStream_t st)
 {
     return bf16 ? sm::launch_typed<true>(x, y, rows, cols, st) : sm::launch_typed<false>(x, y, rows, cols, st);
+}
+
+cudaError_t read_and_clear_softmax_status(uint32_t *word)
+{
+    unsigned int w = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&w, g_softmax_status, sizeof(w));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_softmax_status, &zero, sizeof(zero));
+    if (word) *word = w;
+    return e;
 }
 
 } // namespace fa

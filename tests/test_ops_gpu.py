@@ -92,8 +92,11 @@ def check_softmax(y_gpu, ref, bf16, what):
     assert (err <= tol).all(), f"{what}: worst excess {(err - tol).max():.3e}"
 
 
-SOFTMAX_SHAPES = [(1, 1), (3, 7), (1000, 33), (5, 129), (64, 1000), (9, 1024), (10, 4096), (3, 8200),
-                  (2, 16384), (2, 20000), (4, 65544)]
+# every path: register groups of 32 .. 256 threads with 1 .. 8 vectors, the shared-memory path
+# with two and one row buffers, the vectorised and scalar two-pass paths, ragged widths
+SOFTMAX_SHAPES = [(1, 1), (3, 7), (7, 8), (1000, 33), (33, 256), (5, 129), (64, 1000), (9, 1024), (6, 2048),
+                  (10, 4096), (3, 8200), (2, 16384), (2, 20000), (3, 32768), (2, 50000), (2, 60000), (4, 65544),
+                  (1, 262144), (2, 70001)]
 
 
 @pytest.mark.parametrize("bf16", [False, True])
