@@ -39,6 +39,7 @@ namespace one {
 constexpr int BM = 128, BN = 64;
 constexpr int THREADS = 256;
 constexpr float kTau = 8.0f;
+constexpr uint32_t kNegateA = 1u << 13;  // instruction-descriptor bit: negate A (scale < 0 -> S = -Q K^T)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 enum Site : uint32_t { S_EMPTY = 1, S_Q = 2, S_FULL = 3, S_P = 4, S_S = 5, S_PV = 6, S_DRAIN = 7, S_QFREE = 8, S_SMEM = 9 };
@@ -197,9 +198,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     !bounded_wait(bar_qfree(buf), ((tau / C::NQ) - 1) & 1, abort_flag, tmo, S_QFREE, status))
                     break;
                 mbar_arrive_expect_tx(bar_q(buf), C::QTILE);
+                // scale == 0: every score is 0, so load Q from a plane past the end of the
+                // tensor, which the copy engine fills with zeros
+                const int zq = p.smode == 2 ? p.B * p.Hq : u.zq;
 #pragma unroll
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d(sQ + buf * C::QTILE + pn * C::QPANEL, &tmQ, pn * 64, u.t * BM, u.zq, bar_q(buf));
+                    tma_load_3d(sQ + buf * C::QTILE + pn * C::QPANEL, &tmQ, pn * 64, u.t * BM, zq, bar_q(buf));
                 ++tau;
             }
             for (int x = max(0, tau - C::NQ); x < tau; ++x)
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (whole warp)
-        constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false);
+        const uint32_t idS = idesc_f16(BF16, BM, BN, false) | (p.smode == 1 ? kNegateA : 0u);
         constexpr uint32_t idPV = idesc_f16(BF16, BM, D, true);
         constexpr uint32_t HI = sdesc_hi_sw128(1024);
         auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) {
@@ -310,13 +314,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     reg_fence_x32(v1);
                 }
                 float *s = reinterpret_cast<float *>(sv);
-                if (p.smode == 1) {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) s[c] = -s[c];
-                } else if (p.smode == 2) {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) s[c] = 0.f;
-                }
                 const int kbase = j * BN;
                 const bool tail = kbase + BN > p.Sk;
                 const bool diag = CAUSAL && (kbase + BN - 1 > u.t * BM + p.coff);

@@ -54,6 +54,7 @@ constexpr uint32_t kRegsLoad = 88;    // warps 0-3 after setmaxnreg.dec
 constexpr uint32_t kRegsSoftmax = 208;// warps 4-11 after setmaxnreg.inc: 88*128 + 208*256 == 168*384
 static_assert(kRegsLoad * 128 + kRegsSoftmax * 256 == kRegsLaunch * kThreads, "register split");
 constexpr float kTau = 8.0f;          // lazy-rescale threshold in log2 units (factor 256)
+constexpr uint32_t kNegateA = 1u << 13;  // instruction-descriptor bit: negate A (scale < 0 -> S = -Q K^T)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 enum WaitSite : uint32_t {
@@ -248,9 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(bar_q(buf), C::TILE);
                     const int t = x ? u.tB : u.tA;
+                    // scale == 0: every score is 0, so load Q from a plane past the end of the
+                    // tensor, which the copy engine fills with zeros
+                    const int zq = p.smode == 2 ? p.B * p.Hq : u.zq;
 #pragma unroll
                     for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d(sQ + buf * C::TILE + pn * C::PANEL, &tmQ, pn * 64, t * kBM, u.zq, bar_q(buf));
+                        tma_load_3d(sQ + buf * C::TILE + pn * C::PANEL, &tmQ, pn * 64, t * kBM, zq, bar_q(buf));
                     ++tau;
                 }
             }
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ======================================================== MMA issuer
             // The whole warp runs this loop in uniform control flow (so descriptors live in
             // uniform registers); one elected lane issues each tcgen05 instruction.
-            constexpr uint32_t idS = idesc_f16(BF16, kBM, kBN, false);
+            const uint32_t idS = idesc_f16(BF16, kBM, kBN, false) | (p.smode == 1 ? kNegateA : 0u);
             constexpr uint32_t idPV = idesc_f16(BF16, kBM, D, true);
             constexpr uint32_t HI = sdesc_hi_sw128(1024);   // 8-row groups 1024 bytes apart
             const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
@@ -413,14 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reg_fence_x32(v3);
                 }
                 float *s = reinterpret_cast<float *>(sv);
-
-                if (p.smode == 1) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) s[c] = -s[c];
-                } else if (p.smode == 2) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) s[c] = 0.f;
-                }
 
                 // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal).
                 const int kbase = j * kBN;

@@ -172,14 +172,19 @@ def test_large_logit_rows(fa, orc, seed, causal):
         check(o, lse, o_ref, l_ref, f"{w}")
 
 
-def test_scale_variants(fa, orc):
-    """Non-default scales, including 0 (uniform weights) and a negative one."""
-    for scale in (0.0, -0.3, 0.9):
-        w = Workload("scale", 1, 4, 2, 300, 300, 128, "bf16", True, 7, scale=scale)
+@pytest.mark.parametrize("kernel,D,dtype,causal,sq,sk", [
+    (1, 128, "bf16", 1, 300, 300), (1, 128, "fp16", 0, 257, 300), (1, 64, "bf16", 2, 400, 150),
+    (2, 128, "fp16", 1, 300, 300), (2, 256, "bf16", 2, 300, 200), (2, 256, "fp16", 0, 130, 333),
+])
+def test_scale_variants(fa, orc, kernel, D, dtype, causal, sq, sk):
+    """Non-default scales on both kernels: 0 (uniform weights over the allowed keys; rows
+    with no allowed key stay empty) and negative ones (the scores change sign)."""
+    for scale in (0.0, -0.3, -0.05, 0.9):
+        w = Workload("scale", 1, 4, 2, sq, sk, D, dtype, causal, 7, scale=scale)
         q, k, v = make_qkv(w)
-        o, lse = run_gpu(fa, w, q, k, v)
-        o_ref, l_ref = orc.full(q, k, v, False, True, scale)
-        check(o, lse, o_ref, l_ref, f"scale={scale}")
+        o, lse = run_gpu(fa, w, q, k, v, kernel=kernel)
+        o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, scale)
+        check(o, lse, o_ref, l_ref, f"kernel {kernel} D={D} {dtype} causal={causal} scale={scale}")
 
 
 def test_canaries_untouched(fa):
