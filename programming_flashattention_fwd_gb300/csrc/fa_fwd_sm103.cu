@@ -454,27 +454,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_used = m_new;
                     rescale = true;
                 }
-                // Lazy correction of O (this row's previous P V products are complete: the
-                // S MMA that produced this tile was issued after them).
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t ov[32];
-                        tmem_ld_x32(tO + c, ov);
-                        tmem_wait_ld();
-                        reg_fence_x32(ov);
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float lo, hi;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2), lo, hi);
-                            ov[e] = __float_as_uint(lo);
-                            ov[e + 1] = __float_as_uint(hi);
-                        }
-                        tmem_st_x32(tO + c, ov);
-                    }
-                }
-
                 const float msub = (m_used == -INFINITY) ? 0.f : m_used;
                 const uint64_t negm2 = f2_pack(-msub, -msub);
                 // p = exp2(s*sl2 - m) for 32 keys -> 16 packed 16-bit pairs; l accumulates fp32 p
@@ -507,6 +486,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_x16(tS + 0, pk0);
                     exp_chunk(1, pk1);
                     tmem_st_x16(tS + 16, pk1);
+                    // Lazy correction of O (this row's previous P V products are complete: the
+                    // S MMA that produced this tile was issued after them); it only has to land
+                    // before the first half of P is published, so the vote waits until here.
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t ov[32];
+                            tmem_ld_x32(tO + c, ov);
+                            tmem_wait_ld();
+                            reg_fence_x32(ov);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                float lo, hi;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), a2), lo, hi);
+                                ov[e] = __float_as_uint(lo);
+                                ov[e + 1] = __float_as_uint(hi);
+                            }
+                            tmem_st_x32(tO + c, ov);
+                        }
+                    }
                     exp_chunk(2, pk2);
                     publish(barP);
                     tmem_st_x16(tS + 32, pk2);
