@@ -17,7 +17,7 @@
 //   warp 0       TMA producer of K / V tiles in the order the MMAs consume them (K_0, K_1,
 //                V_0, K_2, V_1, ...), into a ring of 64-row slots
 //   warp 1       TMEM owner and MMA issuer (whole warp; one elected lane issues)
-//   warp 2       TMA producer of query tiles into two rotating buffers
+//   warp 2       TMA producer of query tiles (two rotating buffers at D = 128, one at D = 256)
 //   warps 4-7    softmax / lazy correction / epilogue, one thread per query row
 //
 // The softmax consumes every P V completion in order: before publishing P(j) it waits for
@@ -51,8 +51,12 @@ struct Cfg {
     static constexpr int PANELS = D / 64;
     static constexpr int QPANEL = BM * 128;        // 16 KB
     static constexpr int KVPANEL = BN * 128;       // 8 KB
-    static constexpr int NQ = 2;
-    static constexpr int NS = (D == 256) ? 3 : 8;
+    // D = 256: one query buffer and a five-slot K/V ring.  With two query buffers only three
+    // 32 KB slots fit, one tile of lookahead, and the MMAs wait for K/V loads (+6 % causal,
+    // +12 % non-causal measured for the deeper ring); the next tile's Q load then starts when
+    // this tile's last S MMA has read its buffer.
+    static constexpr int NQ = (D == 256) ? 1 : 2;
+    static constexpr int NS = (D == 256) ? 5 : 8;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * QTILE;
     static constexpr int OFF_BAR = OFF_RING + NS * KVTILE;
