@@ -300,25 +300,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
                 const int nt = 2;                      // tile slots; a slot with nk == 0 has no work
                 const int nk[2] = {u.nA, u.nB};
-                int buf[2] = {0, 0}, na = 0;
+                int buf[2] = {0, 0}, qi[2] = {0, 0}, na = 0;
                 for (int x = 0; x < 2; ++x) {
                     if (nk[x] == 0) continue;
-                    buf[x] = (tau + na) % C::NQ;
-                    ok = ok && wait_u(bar_q(buf[x]), ((tau + na) / C::NQ) & 1, SITE_MMA_Q);
+                    qi[x] = tau + na;
+                    buf[x] = qi[x] % C::NQ;
                     ++na;
                 }
                 tau += na;
                 if (na == 0) continue;                 // no query row of this unit has a key
                 const int uK0 = use;
-                if (ok) ok = wait_u(bar_full(uK0 % C::NS), (uK0 / C::NS) & 1, SITE_MMA_FULL);
-                if (!ok) break;
-                tc_fence_after();
+                if (!wait_u(bar_full(uK0 % C::NS), (uK0 / C::NS) & 1, SITE_MMA_FULL)) {
+                    ok = false;
+                    break;
+                }
                 for (int x = 0; x < nt; ++x) {
                     if (nk[x] == 0) continue;
+                    // each tile's first S goes out as soon as its own Q tile is in (tile b's Q is
+                    // the one loaded last, into the buffer tile a of the previous unit released)
+                    if (!wait_u(bar_q(buf[x]), (qi[x] / C::NQ) & 1, SITE_MMA_Q)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     issue_s(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE);
                     tc_commit_elect(barS0 + 8u * x);
                     if (nk[x] == 1) tc_commit_elect(bar_qfree(buf[x]));
                 }
+                if (!ok) break;
                 tc_commit_elect(bar_empty(uK0 % C::NS));
                 for (int j = 0; j < u.n; ++j) {
                     const bool more = j + 1 < u.n;
