@@ -107,7 +107,7 @@ def kernel_source_hash(kernel: str) -> str:
 def attention_kernel(w, kernel: int) -> str:
     """The kernel fa_fwd_select runs for this workload and variant (0 = automatic)."""
     k = kernel or (2 if w.D == 256 else 1)
-    return "fa::fa_fwd1_kernel" if k == 2 else "fa::fa_fwd_kernel"
+    return "fa::fa_fwd1_kernel" if k >= 2 else "fa::fa_fwd_kernel"
 
 
 def measured_peaks():
@@ -651,8 +651,9 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=90.0, help="reference-arm total budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
-                    help="attention kernel variant: 0 automatic, 1 two tiles / 128-key steps, 2 one tile / 64-key steps")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="attention kernel variant: 0 automatic, 1 two tiles / 128-key steps, "
+                         "2 one tile / 64-key steps, 3 one tile / 128-key steps (D 128)")
     ap.add_argument("--chunks", type=int, default=0,
                     help="pipeline depth of the host-memory (e2e) call; 0 = the library's default")
     ap.add_argument("--op", default="attention", choices=["attention", "gemm", "gemm_gelu", "softmax"])

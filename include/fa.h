@@ -93,6 +93,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *   kernel 2: one 128-row query tile per CTA, 64-key steps, double-buffered scores (D 128 or 256;
  *             the block-size trade of the guide's troubleshooting item, and the only layout
  *             that fits D = 256 in tensor memory)
+ *   kernel 3: one 128-row query tile per CTA, 128-key steps, double-buffered scores (D 128)
  * An unsupported (kernel, D) pair returns FA_ERR_UNSUPPORTED_D; kernel or dtype out of range
  * returns FA_ERR_ARG.
  */

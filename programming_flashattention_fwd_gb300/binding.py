@@ -162,7 +162,8 @@ def fa_fwd_debug(q, k, v, o, lse, causal: bool, scale: float, timeout_ns: int = 
 
 def fa_fwd_select(q, k, v, o, lse, causal, scale: float, kernel: int = 0, stream=None) -> None:
     """The forward with an explicit kernel variant (0 automatic, 1 two query tiles per CTA
-    with 128-key steps, 2 one query tile per CTA with 64-key steps); bf16 or fp16."""
+    with 128-key steps, 2 one query tile per CTA with 64-key steps, 3 one query tile per CTA
+    with 128-key steps, D 128 only); bf16 or fp16."""
     _call("fa_fwd_select", q, k, v, o, lse, causal, scale, stream,
           extra=(int(q.dtype == torch.float16), int(kernel)))
 

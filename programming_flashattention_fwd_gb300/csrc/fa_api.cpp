@@ -84,10 +84,11 @@ int check_fwd_args(const void *q, const void *k, const void *v, const void *o, c
 {
     if (B < 0 || Sq < 0 || Sk < 0) return FA_ERR_BAD_DIM;
     if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_HEADS;
-    if (kernel < 0 || kernel > 2) return FA_ERR_ARG;
+    if (kernel < 0 || kernel > 3) return FA_ERR_ARG;
     if (kernel == 0) kernel = (D == 256) ? 2 : 1;
     if (kernel == 1 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
     if (kernel == 2 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED_D;
+    if (kernel == 3 && D != 128) return FA_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
     if (causal < 0 || causal > 2) return FA_ERR_CAUSAL;
     if (B == 0 || Sq == 0) return FA_OK;
@@ -111,7 +112,8 @@ int check_fwd_args(const void *q, const void *k, const void *v, const void *o, c
 namespace {
 
 // kernel: 0 = automatic (two-tile for D <= 128, one-tile for D = 256), 1 = two query tiles per
-// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 128 / 256).
+// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 128 / 256),
+// 3 = one query tile per CTA with 128-key steps (D 128); kernels 2 and 3 double-buffer the scores.
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
         int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject,
         int kernel = 0)
@@ -123,7 +125,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     }
     if (kernel == 0) kernel = (D == 256) ? 2 : 1;
     const long long BHq = (long long)B * Hq, BHkv = (long long)B * Hkv;
-    const int key_tile = kernel == 2 ? 64 : fa::kBN;
+    const int key_tile = kernel == 2 ? 64 : fa::kBN;   // keys per step of the chosen kernel
     const long long Tq = (Sq + fa::kBM - 1) / fa::kBM, Tk = (Sk + key_tile - 1) / key_tile;
     const long long NP = (Tq + 1) / 2;
 
@@ -155,7 +157,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.Tk = (int)Tk;
     p.NP = (int)NP;
     p.group = Hq / Hkv;
-    p.num_units = (int)(kernel == 2 ? BHq * Tq : BHq * NP);
+    p.num_units = (int)(kernel >= 2 ? BHq * Tq : BHq * NP);
     // The kernel masks keys with -inf scores and takes the row maximum before scaling, so it
     // needs a positive multiplier: a negative scale negates the scores instead, and a zero
     // scale replaces every score by 0 (uniform weights), both exactly.
@@ -166,7 +168,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.inject = inject;
     p.o_al32 = aligned(o, 32) ? 1u : 0u;   // rows are 2*D bytes, so every row then starts on 32 bytes
 
-    cudaError_t e = kernel == 2 ? fa::launch_fwd1(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream))
+    cudaError_t e = kernel >= 2 ? fa::launch_fwd1(D, key_tile, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream))
                                 : fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }

@@ -1,21 +1,21 @@
-// fa_fwd1_sm103.cu -- FlashAttention forward, one query tile per CTA, 64-key tiles, with
-// double-buffered scores in tensor memory: the variant for head dimension 256 (and a 64-key
-// alternative for D = 128).  Same computation as fa_fwd_sm103.cu (the flash-attention
+// fa_fwd1_sm103.cu -- FlashAttention forward, one query tile per CTA, with double-buffered
+// scores in tensor memory: the variant for head dimension 256 (64-key steps) and two
+// alternatives for D = 128 (64- or 128-key steps).  Same computation as fa_fwd_sm103.cu (the flash-attention
 // section of "Guia Prático de Programação de GPU com Tiles"; the FlashAttention-4 features of
 // "Como Domar o Blackwell Sem Enlouquecer com CUDA"); the guide's troubleshooting item trades
 // the 128-row block for 64 to save memory, which is what the key tile does here.
 //
 // With D = 256 the two-tile layout of the main kernel no longer fits in TMEM (2 x 128 score
 // columns + 2 x 256 accumulator columns > 512).  Instead one 128-row query tile owns
-//   S_0 [0,64)  S_1 [64,128)   fp32 scores of two consecutive key tiles; P (16-bit pairs)
-//                              overwrites the first 32 columns of its S
-//   O   [128, 128+D)           fp32 accumulator
+//   S_0 [0,BN)  S_1 [BN,2BN)   fp32 scores of two consecutive key tiles of BN keys; P (16-bit
+//                              pairs) overwrites the first BN/2 columns of its S
+//   O   [2BN, 2BN+D)           fp32 accumulator
 // and the MMA warp computes S(j+1) = Q K_{j+1}^T while the softmax works on S(j); then
 // O += P(j) V_j.  Per 64-key step the tensor pipe has 2 x 128*64*D multiply-adds (1024 cycles
 // at D = 256), which the softmax of 64 keys per row fits under.
 //
 //   warp 0       TMA producer of K / V tiles in the order the MMAs consume them (K_0, K_1,
-//                V_0, K_2, V_1, ...), into a ring of 64-row slots
+//                V_0, K_2, V_1, ...), into a ring of BN-row slots
 //   warp 1       TMEM owner and MMA issuer (whole warp; one elected lane issues)
 //   warp 2       TMA producer of query tiles (two rotating buffers at D = 128, one at D = 256)
 //   warps 4-7    softmax / lazy correction / epilogue, one thread per query row
@@ -36,7 +36,7 @@ __device__ unsigned int g_fa1_status;
 
 namespace one {
 
-constexpr int BM = 128, BN = 64;
+constexpr int BM = 128;
 constexpr int THREADS = 256;
 constexpr float kTau = 8.0f;
 constexpr uint32_t kNegateA = 1u << 13;  // instruction-descriptor bit: negate A (scale < 0 -> S = -Q K^T)
@@ -44,19 +44,25 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 enum Site : uint32_t { S_EMPTY = 1, S_Q = 2, S_FULL = 3, S_P = 4, S_S = 5, S_PV = 6, S_DRAIN = 7, S_QFREE = 8, S_SMEM = 9 };
 
-template <int D>
+// BN keys per step: 64 (the only width at D = 256 whose two score buffers and O fit TMEM; at
+// D = 128 the smaller-tile variant) or 128 (D = 128: the same step as the two-tile kernel).
+constexpr int KVTILE_BYTES(int D, int BN) { return BN * D * 2; }
+
+template <int D, int BN_>
 struct Cfg {
+    static constexpr int BN = BN_;
     static constexpr int QTILE = BM * D * 2;       // 128 rows
-    static constexpr int KVTILE = BN * D * 2;      // 64 rows
+    static constexpr int KVTILE = BN * D * 2;      // BN rows
     static constexpr int PANELS = D / 64;
     static constexpr int QPANEL = BM * 128;        // 16 KB
-    static constexpr int KVPANEL = BN * 128;       // 8 KB
+    static constexpr int KVPANEL = BN * 128;       // BN rows of one 64-column panel
     // D = 256: one query buffer and a five-slot K/V ring.  With two query buffers only three
     // 32 KB slots fit, one tile of lookahead, and the MMAs wait for K/V loads (+6 % causal,
     // +12 % non-causal measured for the deeper ring); the next tile's Q load then starts when
-    // this tile's last S MMA has read its buffer.
+    // this tile's last S MMA has read its buffer.  D = 128: two query buffers and as many K/V
+    // slots as fit (eight of 16 KB for 64-key steps, five of 32 KB for 128-key steps).
     static constexpr int NQ = (D == 256) ? 1 : 2;
-    static constexpr int NS = (D == 256) ? 5 : 8;
+    static constexpr int NS = (KVTILE_BYTES(D, BN_) == 16384) ? 8 : 5;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * QTILE;
     static constexpr int OFF_BAR = OFF_RING + NS * KVTILE;
@@ -72,7 +78,7 @@ struct Unit {
     int zq, zkv, t, nk;
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, int BN>
 __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
 {
     const int G = gridDim.x, c = blockIdx.x;
@@ -100,12 +106,13 @@ __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
     return true;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, int KEYS, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_fwd1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, KEYS>;
+    constexpr int BN = C::BN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 return true;
             };
             Unit u;
-            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+            for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
                 if (u.nk == 0) continue;
                 ok = load(&tmK, 0, u.zkv);
                 for (int j = 0; j < u.nk && ok; ++j) {
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int tau = 0;
             bool ok = true;
             Unit u;
-            for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+            for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
                 if (u.nk == 0) continue;
                 const int buf = tau % C::NQ;
                 if (tau >= C::NQ &&
@@ -229,18 +236,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_ss_kk4_elect(dS, qlo + (uint32_t)((pn * C::QPANEL) >> 4), klo + (uint32_t)((pn * C::KVPANEL) >> 4),
                                  HI, idS, pn > 0);
         };
-        // O += P V over 64 keys: A = P from TMEM, B = V (MN-major, 64-column panels 8 KB apart)
+        // O += P V over BN keys: A = P from TMEM, B = V (MN-major, 64-column panels C::KVPANEL
+        // apart); one group of four 16-key steps per 64 keys
         auto issue_pv = [&](uint32_t tP, uint32_t sV, bool first) {
             const uint32_t vlo = sdesc_lo(sV, C::KVPANEL);
-            static_assert(BN == 64, "one four-step group covers the 64 keys");
-            mma_ts_mn4_elect(tmem + C::COL_O, tP, vlo, HI, idPV, first ? 0u : 1u);
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h)
+                mma_ts_mn4_elect(tmem + C::COL_O, tP + 32 * h, vlo + (uint32_t)((4 * h * 2048) >> 4), HI, idPV,
+                                 (first && h == 0) ? 0u : 1u);
         };
         auto tS = [&](uint32_t gs) { return tmem + ((gs & 1) ? C::COL_S1 : C::COL_S0); };
         int use = 0, tau = 0;
         uint32_t g = 0;   // global key step: S buffer g % 2, barS phase (g / 2) & 1, barP / barPV phase g & 1
         bool ok = true;
         Unit u;
-        for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+        for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
             if (u.nk == 0) continue;
             const int buf = tau % C::NQ;
             ok = wait_u(bar_q(buf), (tau / C::NQ) & 1, S_Q);
@@ -289,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t g = 0;
         bool ok = true;
         Unit u;
-        for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+        for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
             const int row = u.t * BM + r;
             uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)u.zq * p.Sq + row) * (size_t)(D * 2);
             if (u.nk == 0) {   // no allowed key for any row of this tile: o = 0, lse = -inf
@@ -308,15 +318,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sv[BN];
-                {
-                    uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 0);
-                    uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32);
-                    tmem_ld_x32(tSb + 0, v0);
-                    tmem_ld_x32(tSb + 32, v1);
-                    tmem_wait_ld();
-                    reg_fence_x32(v0);
-                    reg_fence_x32(v1);
-                }
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) tmem_ld_x32(tSb + c, *reinterpret_cast<uint32_t(*)[32]>(sv + c));
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(sv + c));
                 float *s = reinterpret_cast<float *>(sv);
                 const int kbase = j * BN;
                 const bool tail = kbase + BN > p.Sk;
@@ -328,8 +334,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int c = 0; c < BN; ++c)
                         if (c > lim) s[c] = -INFINITY;
                 }
-                // row maximum: eight chains seeded with 16 scores, then 3 rounds of 16 (== 64)
-                static_assert(BN == 64, "row-max chains cover 64 scores");
+                // row maximum: eight chains seeded with 16 scores, then rounds of 16 more
+                static_assert(BN % 16 == 0 && BN >= 32, "row-max chains cover the step exactly");
                 float mx[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) lsum2[i] = f2_pack(0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < BN / 32; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -453,10 +459,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, int KEYS, bool BF16, bool CAUSAL>
 static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t stream)
 {
-    auto kern = fa_fwd1_kernel<D, BF16, CAUSAL>;
+    auto kern = fa_fwd1_kernel<D, KEYS, BF16, CAUSAL>;
     static std::atomic<uint64_t> configured{0};
     static std::atomic<int> sm_count[64];
     int dev = 0;
@@ -465,7 +471,7 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << dev;
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::ALLOC);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, KEYS>::ALLOC);
         if (e != cudaSuccess) return e;
         int nsm = 0;
         e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -476,18 +482,19 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
     Params q = p;
     if (q.timeout_ns == 0) q.timeout_ns = kDefaultTimeoutNs;
     const int grid = min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
-    kern<<<grid, THREADS, Cfg<D>::ALLOC, stream>>>(m.q, m.k, m.v, q);
+    kern<<<grid, THREADS, Cfg<D, KEYS>::ALLOC, stream>>>(m.q, m.k, m.v, q);
     return cudaGetLastError();
 }
 
 } // namespace one
 
-cudaError_t launch_fwd1(int D, bool bf16, bool causal, const Maps &m, const Params &p, cudaStream_t st)
+cudaError_t launch_fwd1(int D, int keys, bool bf16, bool causal, const Maps &m, const Params &p, cudaStream_t st)
 {
-#define F1_CASE(DD, BB, CC) \
-    if (D == DD && bf16 == BB && causal == CC) return one::launch_one<DD, BB, CC>(m, p, st);
-    F1_CASE(128, true, false) F1_CASE(128, true, true) F1_CASE(128, false, false) F1_CASE(128, false, true)
-    F1_CASE(256, true, false) F1_CASE(256, true, true) F1_CASE(256, false, false) F1_CASE(256, false, true)
+#define F1_CASE(DD, KK, BB, CC) \
+    if (D == DD && keys == KK && bf16 == BB && causal == CC) return one::launch_one<DD, KK, BB, CC>(m, p, st);
+    F1_CASE(128, 64, true, false) F1_CASE(128, 64, true, true) F1_CASE(128, 64, false, false) F1_CASE(128, 64, false, true)
+    F1_CASE(128, 128, true, false) F1_CASE(128, 128, true, true) F1_CASE(128, 128, false, false) F1_CASE(128, 128, false, true)
+    F1_CASE(256, 64, true, false) F1_CASE(256, 64, true, true) F1_CASE(256, 64, false, false) F1_CASE(256, 64, false, true)
 #undef F1_CASE
     return cudaErrorInvalidValue;
 }

@@ -35,6 +35,7 @@ def test_attention_kernel_choice_follows_head_dim():
     assert bench.attention_kernel(w128, 0) == "fa::fa_fwd_kernel"
     assert bench.attention_kernel(w256, 0) == "fa::fa_fwd1_kernel"
     assert bench.attention_kernel(w128, 2) == "fa::fa_fwd1_kernel"
+    assert bench.attention_kernel(w128, 3) == "fa::fa_fwd1_kernel"
 
 
 def test_committed_profiles_match_the_current_sources():

@@ -112,36 +112,36 @@ def test_shape_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
 
 
 SWEEP_ONE = []
-for D in (128, 256):
+for D, kernel in ((128, 2), (256, 0), (128, 3)):
     for (B, Hq, Hkv, Sq, Sk) in [(1, 1, 1, 1, 1), (1, 2, 1, 63, 63), (1, 2, 2, 64, 65), (2, 4, 2, 129, 129),
                                  (1, 3, 3, 300, 300), (1, 4, 2, 384, 200), (1, 2, 1, 200, 384),
                                  (1, 2, 1, 513, 100), (1, 2, 2, 1, 300)]:
         for causal in (0, 1, 2):
-            SWEEP_ONE.append((B, Hq, Hkv, Sq, Sk, D, causal))
+            SWEEP_ONE.append((B, Hq, Hkv, Sq, Sk, D, causal, kernel))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal", SWEEP_ONE)
-def test_one_tile_kernel_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
-    """The one-query-tile kernel (64-key steps): D = 256 through the automatic choice, D = 128
-    through fa_fwd_select(kernel=2); every row checked."""
-    seed = zlib.crc32(repr(("one", B, Hq, Hkv, Sq, Sk, D, causal, dtype)).encode()) % 100000
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,kernel", SWEEP_ONE)
+def test_one_tile_kernel_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal, kernel):
+    """The one-query-tile kernel: 64-key steps at D = 256 (the automatic choice) and at D = 128
+    (fa_fwd_select kernel 2), 128-key steps at D = 128 (kernel 3); every row checked."""
+    seed = zlib.crc32(repr(("one", B, Hq, Hkv, Sq, Sk, D, causal, dtype) + ((kernel,) if kernel == 3 else ())).encode()) % 100000
     w = Workload("sweep1", B, Hq, Hkv, Sq, Sk, D, dtype, causal, seed,
                  q_std=2.0 if dtype == "fp16" else 1.0, k_std=2.0 if dtype == "fp16" else 1.0)
     q, k, v = make_qkv(w)
-    o, lse = run_gpu(fa, w, q, k, v, kernel=0 if D == 256 else 2)
+    o, lse = run_gpu(fa, w, q, k, v, kernel=kernel)
     o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
-    check(o, lse, o_ref, l_ref, f"{w}")
+    check(o, lse, o_ref, l_ref, f"{w} kernel {kernel}")
 
 
 def test_kernel_variants_agree_at_d128(fa, orc):
-    """Both kernels serve D = 128: each matches the oracle on the bench shape's rows."""
+    """Three kernels serve D = 128: each matches the oracle on the bench shape's rows."""
     w = WORKLOADS["gqa_causal_b2_h32kv8_s4096"]
     q, k, v = make_qkv(w)
     rows = sample_rows(w, n=128)
     o_ref, l_ref = orc.rows(q, k, v, False, w.causal, w.softmax_scale, rows)
     r = torch.from_numpy(rows)
-    for kernel in (1, 2):
+    for kernel in (1, 2, 3):
         o, lse = run_gpu(fa, w, q, k, v, kernel=kernel)
         check(o.cpu()[r[:, 0], r[:, 1], r[:, 2]], lse.cpu()[r[:, 0], r[:, 1], r[:, 2]], o_ref, l_ref, f"kernel {kernel}")
 
@@ -175,9 +175,10 @@ def test_large_logit_rows(fa, orc, seed, causal):
 @pytest.mark.parametrize("kernel,D,dtype,causal,sq,sk", [
     (1, 128, "bf16", 1, 300, 300), (1, 128, "fp16", 0, 257, 300), (1, 64, "bf16", 2, 400, 150),
     (2, 128, "fp16", 1, 300, 300), (2, 256, "bf16", 2, 300, 200), (2, 256, "fp16", 0, 130, 333),
+    (3, 128, "bf16", 2, 300, 200), (3, 128, "fp16", 1, 257, 257),
 ])
 def test_scale_variants(fa, orc, kernel, D, dtype, causal, sq, sk):
-    """Non-default scales on both kernels: 0 (uniform weights over the allowed keys; rows
+    """Non-default scales on every kernel: 0 (uniform weights over the allowed keys; rows
     with no allowed key stay empty) and negative ones (the scores change sign)."""
     for scale in (0.0, -0.3, -0.05, 0.9):
         w = Workload("scale", 1, 4, 2, sq, sk, D, dtype, causal, 7, scale=scale)
@@ -204,7 +205,7 @@ def test_canaries_untouched(fa):
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 
-@pytest.mark.parametrize("kernel,D", [(1, 64), (1, 128), (2, 128), (2, 256)])
+@pytest.mark.parametrize("kernel,D", [(1, 64), (1, 128), (2, 128), (2, 256), (3, 128)])
 @pytest.mark.parametrize("offset", [8, 16])
 def test_output_alignment_paths(fa, orc, kernel, D, offset):
     """o 32-byte aligned (rows written in 32-byte sectors) or only 16-byte aligned (16-byte
