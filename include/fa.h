@@ -120,14 +120,19 @@ int fa_device_status(fa_stream_t stream, uint32_t *detail);
 
 /*
  * fa_fwd_debug -- test hook: fa_fwd / fa_fwd_fp16 (is_fp16 selects) with an explicit
- * watchdog limit per wait (timeout_ns, 0 = the default of 2 s) and a fault-injection mask
+ * watchdog limit per wait (timeout_ns, 0 = the default of 2 s), a fault-injection mask
  * (inject bit 0: the load warp skips the first V tile, so the MMA warp's wait for it
- * expires; the kernel then records FA_ERR_DEVICE_TIMEOUT and every CTA returns normally).
- * With inject == 0 and timeout_ns == 0 it is exactly fa_fwd / fa_fwd_fp16.
+ * expires; the kernel then records FA_ERR_DEVICE_TIMEOUT and every CTA returns normally),
+ * the kernel variant (as fa_fwd_select) and the lazy-rescale threshold tau in log2 units
+ * (O and l are rescaled only when the running row maximum grows by more than tau; 0 rescales
+ * at every new maximum; negative = the default 8; above 15 -- where an unnormalised P could
+ * leave the fp16 range -- or NaN returns FA_ERR_ARG).
+ * With inject == 0, timeout_ns == 0, kernel == 0 and tau < 0 it is exactly fa_fwd / fa_fwd_fp16.
  */
 int fa_fwd_debug(const void *q, const void *k, const void *v, void *o, float *lse,
                  int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
-                 fa_stream_t stream, int is_fp16, uint64_t timeout_ns, uint32_t inject);
+                 fa_stream_t stream, int is_fp16, uint64_t timeout_ns, uint32_t inject,
+                 int kernel, float tau);
 
 /*
  * fa_gemm -- tiled matrix product with an optional fused epilogue, the tutorial's building

@@ -45,7 +45,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.fa_fwd_select.restype = ctypes.c_int
     lib.fa_fwd_select.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_int]
     lib.fa_fwd_debug.restype = ctypes.c_int
-    lib.fa_fwd_debug.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
+    lib.fa_fwd_debug.argtypes = _FWD_ARGS + [ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int, ctypes.c_float]
     lib.fa_fwd_host.restype = ctypes.c_int
     lib.fa_fwd_host.argtypes = ([ctypes.c_void_p] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
                                                                                 ctypes.c_int, ctypes.c_void_p])
@@ -154,10 +154,11 @@ def fa_fwd_fp16(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> Non
 
 
 def fa_fwd_debug(q, k, v, o, lse, causal: bool, scale: float, timeout_ns: int = 0,
-                 inject: int = 0, stream=None) -> None:
-    """Test hook: the forward with an explicit watchdog limit and fault-injection mask."""
+                 inject: int = 0, kernel: int = 0, tau: float = -1.0, stream=None) -> None:
+    """Test hook: the forward with an explicit watchdog limit, fault-injection mask, kernel
+    variant and lazy-rescale threshold tau (log2 units; negative = the default 8)."""
     _call("fa_fwd_debug", q, k, v, o, lse, causal, scale, stream,
-          extra=(int(q.dtype == torch.float16), int(timeout_ns), int(inject)))
+          extra=(int(q.dtype == torch.float16), int(timeout_ns), int(inject), int(kernel), float(tau)))
 
 
 def fa_fwd_select(q, k, v, o, lse, causal, scale: float, kernel: int = 0, stream=None) -> None:

@@ -116,7 +116,7 @@ namespace {
 // 3 = one query tile per CTA with 128-key steps (D 128); kernels 2 and 3 double-buffer the scores.
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
         int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject,
-        int kernel = 0)
+        int kernel = 0, float tau = fa::kTauDefault)
 {
     // ---- argument checks: no CUDA call before these pass
     {
@@ -167,6 +167,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.timeout_ns = timeout_ns;
     p.inject = inject;
     p.o_al32 = aligned(o, 32) ? 1u : 0u;   // rows are 2*D bytes, so every row then starts on 32 bytes
+    p.tau = tau;
 
     cudaError_t e = kernel >= 2 ? fa::launch_fwd1(D, key_tile, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream))
                                 : fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));
@@ -263,9 +264,13 @@ int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse
 
 int fa_fwd_debug(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
                  int Sk, int D, int causal, float scale, fa_stream_t stream, int is_fp16, uint64_t timeout_ns,
-                 uint32_t inject)
+                 uint32_t inject, int kernel, float tau)
 {
-    return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, is_fp16 == 0, timeout_ns, inject);
+    // negative: the default; above 15 an unnormalised P could leave the fp16 range
+    if (!(tau >= 0.f && tau <= 15.f)) tau = tau < 0.f ? fa::kTauDefault : NAN;
+    if (std::isnan(tau)) return FA_ERR_ARG;
+    return run(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream, is_fp16 == 0, timeout_ns, inject,
+               kernel, tau);
 }
 
 int fa_fwd_select(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,

@@ -38,7 +38,6 @@ namespace one {
 
 constexpr int BM = 128;
 constexpr int THREADS = 256;
-constexpr float kTau = 8.0f;
 constexpr uint32_t kNegateA = 1u << 13;  // instruction-descriptor bit: negate A (scale < 0 -> S = -Q K^T)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -350,7 +349,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bool rescale = false;
                 if (j == 0) {
                     m_used = m_new;
-                } else if (m_new - m_used > kTau) {
+                } else if (m_new - m_used > p.tau) {
                     alpha = ex2_approx(m_used - m_new);
                     l *= alpha;
                     m_used = m_new;

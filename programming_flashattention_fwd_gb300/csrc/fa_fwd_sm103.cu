@@ -53,7 +53,6 @@ constexpr int kRegsLaunch = 168;      // 65536 / 384, rounded down to the alloca
 constexpr uint32_t kRegsLoad = 88;    // warps 0-3 after setmaxnreg.dec
 constexpr uint32_t kRegsSoftmax = 208;// warps 4-11 after setmaxnreg.inc: 88*128 + 208*256 == 168*384
 static_assert(kRegsLoad * 128 + kRegsSoftmax * 256 == kRegsLaunch * kThreads, "register split");
-constexpr float kTau = 8.0f;          // lazy-rescale threshold in log2 units (factor 256)
 constexpr uint32_t kNegateA = 1u << 13;  // instruction-descriptor bit: negate A (scale < 0 -> S = -Q K^T)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -401,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 
-            float m_used = -INFINITY;  // running max in exp2 units (possibly stale by <= kTau)
+            float m_used = -INFINITY;  // running max in exp2 units (possibly stale by <= p.tau)
             float l = 0.f;             // running sum of p at m_used
             for (int j = 0; j < nk; ++j) {
                 ok = __all_sync(0xffffffffu, wait_bar(barS, ks & 1, abort_flag, tmo, SITE_SM_S));
@@ -457,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool rescale = false;
                 if (j == 0) {
                     m_used = m_new;
-                } else if (m_new - m_used > kTau) {
+                } else if (m_new - m_used > p.tau) {
                     alpha = ex2_approx(m_used - m_new);
                     l *= alpha;
                     m_used = m_new;

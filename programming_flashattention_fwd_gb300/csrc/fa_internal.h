@@ -10,6 +10,10 @@ namespace fa {
 // Tile sizes: 128 query rows x 128 keys per step (the guide's default block of 128).
 constexpr int kBM = 128;
 constexpr int kBN = 128;
+// Lazy-rescale threshold in log2 units: O and l are rescaled only when the running maximum grows
+// by more than tau, so unnormalised p stays <= 2^tau (256, well inside the 16-bit ranges).  Any
+// tau >= 0 gives the same result up to rounding; tau = 0 rescales at every new maximum.
+constexpr float kTauDefault = 8.0f;
 
 // Per-launch scalar parameters (passed by value to the kernel).
 struct Params {
@@ -26,6 +30,7 @@ struct Params {
     uint64_t timeout_ns;// watchdog limit of each bounded wait
     uint32_t inject;    // fault-injection mask (0 in normal use)
     uint32_t o_al32;    // o is 32-byte aligned: output rows are written in full 32-byte sectors
+    float tau;          // lazy-rescale threshold (kTauDefault outside tests)
 };
 
 // The TMA descriptors: q, k, v as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.

@@ -111,8 +111,15 @@ def test_overlapping_outputs(lib, over):
 
 def test_debug_entry_point_validates_the_same_way(lib):
     f = lib.fa_fwd_debug
-    assert f(Q, K, V, O, L, 1, 3, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0) == 3
-    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 80, 0, 1.0, None, 1, 0, 0) == 4
+    assert f(Q, K, V, O, L, 1, 3, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0, 0, -1.0) == 3
+    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 80, 0, 1.0, None, 1, 0, 0, 0, -1.0) == 4
+    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 256, 0, 1.0, None, 0, 0, 0, 1, -1.0) == 4   # kernel 1 has no D 256
+    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0, 5, -1.0) == 15  # no kernel 5
+    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0, 0, float("nan")) == 15
+    assert f(Q, K, V, O, L, 1, 2, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0, 0, 15.5) == 15
+    # valid tau values pass validation (the overlapping lse then stops the call before CUDA)
+    for tau in (0.0, 8.0, 15.0, -1.0):
+        assert f(Q, K, V, O, O + 16, 1, 2, 2, 8, 8, 128, 0, 1.0, None, 0, 0, 0, 3, tau) == 6
 
 
 # fa_gemm(a, b, c, bias, M, N, K, dtype, out_fp32, epilogue, stream) -- every call rejected before CUDA

@@ -172,6 +172,31 @@ def test_large_logit_rows(fa, orc, seed, causal):
         check(o, lse, o_ref, l_ref, f"{w}")
 
 
+@pytest.mark.parametrize("kernel,D", [(1, 64), (1, 128), (2, 128), (3, 128), (2, 256)])
+def test_lazy_rescale_threshold(fa, orc, kernel, D):
+    """The result does not depend on the lazy-rescale threshold: tau = 0 (rescale at every new
+    row maximum, the tutorial's recurrence), the default 8 and 15 (P up to 2^15 before a
+    rescale, the most the fp16 range allows) each match the oracle, on large-logit inputs
+    whose row maxima keep growing across key tiles, and the three outputs agree with one
+    another to within the 16-bit rounding of O."""
+    w = Workload("tau", 1, 4, 2, 300, 700, D, "fp16" if D == 64 else "bf16", 1, 31 + D + kernel,
+                 q_std=2.0, k_std=2.0)
+    q, k, v = make_qkv(w)
+    o_ref, l_ref = orc.full(q, k, v, w.is_fp16, w.causal, w.softmax_scale)
+    outs = []
+    for tau in (0.0, 8.0, 15.0):
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        o = torch.full_like(qd, float("nan"))
+        lse = torch.full(qd.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+        fa.fa_fwd_debug(qd, kd, vd, o, lse, w.causal, w.softmax_scale, kernel=kernel, tau=tau)
+        torch.cuda.synchronize()
+        check(o, lse, o_ref, l_ref, f"kernel {kernel} D {D} tau {tau}")
+        outs.append((o.float().cpu(), lse.cpu()))
+    for o_t, l_t in outs[1:]:
+        assert (o_t - outs[0][0]).abs().max().item() <= 2e-2
+        assert (l_t - outs[0][1]).abs().max().item() <= 1e-3
+
+
 @pytest.mark.parametrize("kernel,D,dtype,causal,sq,sk", [
     (1, 128, "bf16", 1, 300, 300), (1, 128, "fp16", 0, 257, 300), (1, 64, "bf16", 2, 400, 150),
     (2, 128, "fp16", 1, 300, 300), (2, 256, "bf16", 2, 300, 200), (2, 256, "fp16", 0, 130, 333),
