@@ -99,6 +99,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return false;
 }
 
+// One arrival on `bar` by one elected lane of the (converged) warp, without a branch.
+__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
 // One work unit, decoded identically by every role.
 struct Unit {
     int zq, zkv;      // q/o head plane (b*Hq + hq) and k/v head plane (b*Hkv + kvh)
@@ -452,16 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
                 const float m_new = fmaxf(m_used, mrow * sl2);
 
-                float alpha = 1.f;
-                bool rescale = false;
-                if (j == 0) {
-                    m_used = m_new;
-                } else if (m_new - m_used > p.tau) {
-                    alpha = ex2_approx(m_used - m_new);
-                    l *= alpha;
-                    m_used = m_new;
-                    rescale = true;
-                }
+                // (branch-free: the warp's softmax step is bound by issue, and branches cost it)
+                const bool rescale = j > 0 && m_new - m_used > p.tau;
+                const float a_new = ex2_approx(m_used - m_new);
+                const float alpha = rescale ? a_new : 1.f;
+                l *= alpha;
+                m_used = (j == 0 || rescale) ? m_new : m_used;
                 const float msub = (m_used == -INFINITY) ? 0.f : m_used;
                 const uint64_t negm2 = f2_pack(-msub, -msub);
                 // p = exp2(s*sl2 - m) for 32 keys -> 16 packed 16-bit pairs; l accumulates fp32 p
@@ -486,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar);
+                    mbar_arrive_elect(bar);
                 };
                 {
                     uint32_t pk0[16], pk1[16], pk2[16], pk3[16];
