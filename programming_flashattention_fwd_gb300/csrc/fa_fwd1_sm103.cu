@@ -316,34 +316,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ok = __all_sync(0xffffffffu, bounded_wait(barS + 8u * (gs & 1), (gs >> 1) & 1, abort_flag, tmo, S_S, status));
                 if (!ok) break;
                 tc_fence_after();
+                // S in 32-column reducing loads: each also returns the maximum of its 32 scores
                 uint32_t sv[BN];
+                float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < BN; c += 32) tmem_ld_x32(tSb + c, *reinterpret_cast<uint32_t(*)[32]>(sv + c));
+                for (int c = 0; c < BN; c += 32)
+                    tmem_ld_red_max_x32(tSb + c, *reinterpret_cast<uint32_t(*)[32]>(sv + c), pm[c / 32]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < BN; c += 32) reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(sv + c));
+                reg_fence_f4(pm[0], pm[1], pm[2], pm[3]);
                 float *s = reinterpret_cast<float *>(sv);
                 const int kbase = j * BN;
                 const bool tail = kbase + BN > p.Sk;
                 const bool diag = CAUSAL && (kbase + BN - 1 > u.t * BM + p.coff);
-                if (tail || diag) {
+                float mrow = fmaxf(fmax3(pm[0], pm[1], pm[2]), pm[3]);
+                if (tail || diag) {   // masked steps: the row maximum over the masked scores
                     int lim = p.Sk - 1 - kbase;
                     if (CAUSAL) lim = min(lim, row + p.coff - kbase);
 #pragma unroll
                     for (int c = 0; c < BN; ++c)
                         if (c > lim) s[c] = -INFINITY;
+                    // eight chains seeded with 16 scores, then rounds of 16 more
+                    static_assert(BN % 16 == 0 && BN >= 32, "row-max chains cover the step exactly");
+                    float mx[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                    for (int c = 16; c + 16 <= BN; c += 16) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+                    }
+                    mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
                 }
-                // row maximum: eight chains seeded with 16 scores, then rounds of 16 more
-                static_assert(BN % 16 == 0 && BN >= 32, "row-max chains cover the step exactly");
-                float mx[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-                for (int c = 16; c + 16 <= BN; c += 16) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
-                }
-                const float mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
                 const float m_new = fmaxf(m_used, mrow * sl2);
                 float alpha = 1.f;
                 bool rescale = false;

@@ -417,48 +417,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ks;
                 tc_fence_after();
 
+                // S in four 32-column loads; each load also returns the maximum of the 32 scores it
+                // read (the reducing TMEM load), so an unmasked step needs no row-max arithmetic.
                 uint32_t sv[kBN];
+                float pm0, pm1, pm2, pm3;
                 {
                     uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 0);
                     uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32);
                     uint32_t(&v2)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 64);
                     uint32_t(&v3)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 96);
-                    tmem_ld_x32(tS + 0, v0);
-                    tmem_ld_x32(tS + 32, v1);
-                    tmem_ld_x32(tS + 64, v2);
-                    tmem_ld_x32(tS + 96, v3);
+                    tmem_ld_red_max_x32(tS + 0, v0, pm0);
+                    tmem_ld_red_max_x32(tS + 32, v1, pm1);
+                    tmem_ld_red_max_x32(tS + 64, v2, pm2);
+                    tmem_ld_red_max_x32(tS + 96, v3, pm3);
                     tmem_wait_ld();
                     reg_fence_x32(v0);
                     reg_fence_x32(v1);
                     reg_fence_x32(v2);
                     reg_fence_x32(v3);
+                    reg_fence_f4(pm0, pm1, pm2, pm3);
                 }
                 float *s = reinterpret_cast<float *>(sv);
 
-                // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal).
+                // Mask keys past Sk (last key tile) and keys after the query row (causal diagonal);
+                // those steps take the row maximum over the masked scores instead.
                 const int kbase = j * kBN;
                 const bool tail = kbase + kBN > p.Sk;
                 const bool diag = CAUSAL && (kbase + kBN - 1 > t * kBM + p.coff);
+                float mrow = fmaxf(fmax3(pm0, pm1, pm2), pm3);
                 if (tail || diag) {
                     int lim = p.Sk - 1 - kbase;
                     if (CAUSAL) lim = min(lim, row + p.coff - kbase);
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (c > lim) s[c] = -INFINITY;
+                    // eight independent chains; 16 scores seed them, then each round of
+                    // three-input max consumes 16 more (16 + 7 * 16 == 128 == kBN)
+                    static_assert(kBN % 16 == 0 && kBN >= 16, "row-max chains cover the tile exactly");
+                    float mx[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                    for (int c = 16; c + 16 <= kBN; c += 16) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+                    }
+                    mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
                 }
-
-                // Row maximum: eight independent chains; 16 scores seed them, then each round of
-                // three-input max consumes 16 more (16 + 7 * 16 == 128 == kBN).
-                static_assert(kBN % 16 == 0 && kBN >= 16, "row-max chains cover the tile exactly");
-                float mx[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-                for (int c = 16; c + 16 <= kBN; c += 16) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
-                }
-                const float mrow = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
                 const float m_new = fmaxf(m_used, mrow * sl2);
 
                 // (branch-free: the warp's softmax step is bound by issue, and branches cost it)
