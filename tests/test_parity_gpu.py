@@ -13,6 +13,8 @@ same (rounded) inputs.
     top-left causal / bottom-right causal (including query tiles with no allowed key at all);
   - a prefill-onto-cache shape (1000 new queries after 3096 cached keys, bottom-right);
   - guard canaries around every output buffer (no write outside o and lse);
+  - 48 seeded random problems over every kernel (shapes, GQA groups, masks, dtypes, negative
+    and non-default scales, input std), every row checked;
   - bitwise determinism and a non-default stream;
   - the watchdog: an injected missing load makes the kernel give up, report
     FA_ERR_DEVICE_TIMEOUT and return; the context stays usable.
@@ -132,6 +134,36 @@ def test_one_tile_kernel_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal, ke
     o, lse = run_gpu(fa, w, q, k, v, kernel=kernel)
     o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
     check(o, lse, o_ref, l_ref, f"{w} kernel {kernel}")
+
+
+def _fuzz_cases(n=48, seed=2024):
+    """Seeded random problems over every kernel: shapes, GQA groups, masks, dtypes, scales and
+    std; sizes small enough for the float64 oracle to check every row in well under a second."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        kernel = int(rng.choice([1, 1, 2, 3]))
+        D = int(rng.choice({1: [64, 128], 2: [128, 256], 3: [128]}[kernel]))
+        Hkv = int(rng.integers(1, 4))
+        Hq = Hkv * int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        Sq = int(rng.integers(1, 700))
+        Sk = int(rng.integers(1, 700))
+        causal = int(rng.integers(0, 3))
+        dtype = str(rng.choice(["bf16", "fp16"]))
+        std = float(rng.choice([0.5, 1.0, 2.0]))
+        scale = float(rng.choice([D ** -0.5, 0.3 * D ** -0.5, 2.0 * D ** -0.5, -D ** -0.5]))
+        cases.append((i, kernel, B, Hq, Hkv, Sq, Sk, D, causal, dtype, std, scale))
+    return cases
+
+
+@pytest.mark.parametrize("i,kernel,B,Hq,Hkv,Sq,Sk,D,causal,dtype,std,scale", _fuzz_cases())
+def test_random_problems(fa, orc, i, kernel, B, Hq, Hkv, Sq, Sk, D, causal, dtype, std, scale):
+    w = Workload("fuzz", B, Hq, Hkv, Sq, Sk, D, dtype, causal, 1000 + i, q_std=std, k_std=std, scale=scale)
+    q, k, v = make_qkv(w)
+    o, lse = run_gpu(fa, w, q, k, v, kernel=kernel)
+    o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, scale)
+    check(o, lse, o_ref, l_ref, f"case {i}: kernel {kernel} {w} scale {scale:.4f}")
 
 
 def test_kernel_variants_agree_at_d128(fa, orc):
