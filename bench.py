@@ -12,7 +12,8 @@ copies q, k, v host->device, runs the attention and copies o and lse back, all i
 events, with the copies of one chunk of heads overlapped with the kernels of another
 (``--chunks`` sets the pipeline depth).  Two calls are kept in flight (alternate steps use their
 own staging buffers, host outputs and stream, so one step's uploads overlap the previous step's
-kernels and downloads); ``serial_ms_per_step`` is the same with one call at a time.
+kernels and downloads; 2 chunks per call unless ``--chunks`` says otherwise);
+``serial_ms_per_step`` is the same with one call at a time (the library's default depth).
 
 ``roofline`` compares the kernel against the measured dense bf16 tensor peak of the pool's
 GB300s (MEASURED_PEAKS.json when present, else the fallback figure, as stated in the line).
@@ -52,6 +53,7 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+E2E_INFLIGHT_CHUNKS = 2      # fa_fwd_host pipeline depth per call when two calls are in flight
 PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
 
 
@@ -397,7 +399,13 @@ def run_ours(args, w, world, rank, local):
     o2 = torch.empty_like(o)
     l2 = torch.empty_like(lse)
 
-    def e2e_step(bufs=(q2, k2, v2, o2, l2), outs=(o_p, l_p), st=stream):
+    # pipeline depth of fa_fwd_host: one call at a time takes the library's default (4 chunks);
+    # with two calls in flight the neighbouring call already fills the link, and 2 chunks per
+    # call measured best (456 against 430 TFLOP/s with 4 on the 4096-token default)
+    chunks_serial = args.chunks
+    chunks_inflight = args.chunks if args.chunks else E2E_INFLIGHT_CHUNKS
+
+    def e2e_step(bufs=(q2, k2, v2, o2, l2), outs=(o_p, l_p), st=stream, chunks=None):
         qd, kd, vd, od, ld = bufs
         oh, lh = outs
         if args.kernel:   # an explicit variant: copies in, the kernel, copies back, one after another
@@ -410,7 +418,7 @@ def run_ours(args, w, world, rank, local):
                 lh.copy_(ld, non_blocking=True)
         else:             # the host-memory entry point: copies and kernels overlapped chunk by chunk
             binding.fa_fwd_host(q_p, k_p, v_p, oh, lh, qd, kd, vd, od, ld, w.causal, w.softmax_scale,
-                                chunks=args.chunks, stream=st)
+                                chunks=chunks_serial if chunks is None else chunks, stream=st)
 
     def timed(run_steps):
         torch.cuda.synchronize(dev)
@@ -443,11 +451,11 @@ def run_ours(args, w, world, rank, local):
         side.wait_event(ev)
         for i in range(args.steps):
             bufs, outs, st = sets[i % 2]
-            e2e_step(bufs, outs, st)
+            e2e_step(bufs, outs, st, chunks_inflight)
         stream.wait_stream(side)
 
     for i in range(max(2, args.warmup)):
-        e2e_step(*sets[i % 2])
+        e2e_step(*sets[i % 2], chunks_inflight)
     t_e2e = timed(pipelined)
     for oh, lh in ((o_p, l_p), (o_p2, l_p2)):
         assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu()), "e2e result differs from the device run"
@@ -469,7 +477,8 @@ def run_ours(args, w, world, rank, local):
         "config": workload_config(w, args),
         "e2e": {"value": flops * world / t_e2e / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
-                "calls_in_flight": 2, "serial_ms_per_step": t_serial * 1e3,
+                "calls_in_flight": 2, "chunks_per_call": chunks_inflight or 4,
+                "serial_chunks_per_call": chunks_serial or 4, "serial_ms_per_step": t_serial * 1e3,
                 "serial_value": flops * world / t_serial / 1e12,
                 "api": "fa_fwd_host" if not args.kernel else "torch copies + fa_fwd_select"},
         "gpu_launches": args.steps,
@@ -655,7 +664,8 @@ def main():
                     help="attention kernel variant: 0 automatic, 1 two tiles / 128-key steps, "
                          "2 one tile / 64-key steps, 3 one tile / 128-key steps (D 128)")
     ap.add_argument("--chunks", type=int, default=0,
-                    help="pipeline depth of the host-memory (e2e) call; 0 = the library's default")
+                    help="pipeline depth of the host-memory (e2e) call; 0 = the library's default one call "
+                         "at a time and 2 per call with two calls in flight")
     ap.add_argument("--op", default="attention", choices=["attention", "gemm", "gemm_gelu", "softmax"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)
