@@ -66,7 +66,8 @@ typedef enum {
     FA_ERR_DEVICE_TIMEOUT = 12, /* (fa_device_status) a bounded device-side wait expired     */
     FA_ERR_CAUSAL = 13,         /* causal not in {0, 1, 2}                                   */
     FA_ERR_SHAPE = 14,          /* (fa_gemm) K or N not a multiple of 8 (16-byte rows)       */
-    FA_ERR_ARG = 15             /* an enum-like argument (dtype, output type, epilogue) is out of range */
+    FA_ERR_ARG = 15,            /* an enum-like argument (dtype, output type, epilogue) is out of range */
+    FA_ERR_TOO_LARGE = 16       /* (fa_fwd_host_noalloc) the problem needs more than FA_HOST_NOALLOC_MAX_BYTES of staging */
 } fa_status_t;
 
 /*
@@ -195,6 +196,38 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, fl
  * be >= 1.  Asynchronous on `stream`.
  */
 int fa_softmax_rows(const void *x, void *y, int rows, int cols, int dtype, fa_stream_t stream);
+
+/* Size of the fixed device staging area of fa_fwd_host_noalloc: 64 MiB. */
+#define FA_HOST_NOALLOC_MAX_BYTES (64ull << 20)
+
+/*
+ * fa_fwd_host_noalloc -- fa_fwd_host for callers that cannot allocate device memory.  The pages
+ * have no counterpart to it: it exists for callers that hold q, k, v, o and lse in host memory
+ * and may not call cudaMalloc themselves -- for instance a plug-in whose host application owns
+ * every device allocation and caps it, or a caller that must not pay for the implicit device
+ * synchronisation an allocation can bring.  fa_fwd_host needs five device buffers from its
+ * caller as the staging area of its copies; this variant takes them instead from one
+ * FA_HOST_NOALLOC_MAX_BYTES array of device memory that is part of the library's device image.
+ * Each GPU on which that image is loaded keeps the array until the process exits.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   q_h .. lse_h, B .. scale, dtype, chunks, stream : as for fa_fwd_host, with the same results
+ *                   (bit-identical: the same kernels run on the same values)
+ * Staging needs |q| + |k| + |v| + |o| + |lse| bytes, each rounded up to 256 bytes
+ * (2 B Hq Sq D + 2 B Hkv Sk D twice + 4 B Hq Sq before rounding); a larger problem returns
+ * FA_ERR_TOO_LARGE.  That check and every argument check are made before any CUDA call.
+ * The first call on a device (with that device current) looks up the array's device address
+ * once (cudaGetSymbolAddress) and keeps it: make that first call before any stream capture
+ * starts.  A failed look-up returns FA_ERR_NO_DEVICE.
+ * Every call on a device shares the one array, and a call leaves its inputs and results
+ * there.  Nothing in it has to start at zero: each call writes every byte it reads.  Calls
+ * that run at the same time on the GPU race on the array: two calls on one stream run in
+ * order, but calls on different streams must be ordered by the caller (an event, a
+ * synchronise).  In particular, fa_fwd_host_noalloc calls kept in flight on two streams at
+ * once, as fa_fwd_host calls with their own buffers may be, give wrong results.
+ */
+int fa_fwd_host_noalloc(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                        int dtype, int chunks, fa_stream_t stream);
 
 #ifdef __cplusplus
 }

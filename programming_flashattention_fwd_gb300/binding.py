@@ -23,7 +23,11 @@ STATUS = {
     4: "FA_ERR_UNSUPPORTED_D", 5: "FA_ERR_ALIGN", 6: "FA_ERR_ALIAS", 7: "FA_ERR_SCALE",
     8: "FA_ERR_NO_DEVICE", 9: "FA_ERR_ARCH", 10: "FA_ERR_TENSORMAP", 11: "FA_ERR_LAUNCH",
     12: "FA_ERR_DEVICE_TIMEOUT", 13: "FA_ERR_CAUSAL", 14: "FA_ERR_SHAPE", 15: "FA_ERR_ARG",
+    16: "FA_ERR_TOO_LARGE",
 }
+
+# FA_HOST_NOALLOC_MAX_BYTES of include/fa.h: the fixed staging area of fa_fwd_host_noalloc.
+HOST_NOALLOC_MAX_BYTES = 64 << 20
 
 _lib = None
 _lock = threading.Lock()
@@ -49,6 +53,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.fa_fwd_host.restype = ctypes.c_int
     lib.fa_fwd_host.argtypes = ([ctypes.c_void_p] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
                                                                                 ctypes.c_int, ctypes.c_void_p])
+    lib.fa_fwd_host_noalloc.restype = ctypes.c_int
+    lib.fa_fwd_host_noalloc.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
+                                                                                     ctypes.c_int, ctypes.c_void_p])
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_strerror.argtypes = [ctypes.c_int]
     lib.fa_device_status.restype = ctypes.c_int
@@ -187,6 +194,31 @@ def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, causal, sc
         q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
         q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(), lse_d.data_ptr(),
         B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_d.dtype == torch.float16), int(chunks),
+        _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, fa_strerror(st))
+
+
+def fa_fwd_host_noalloc(q_h, k_h, v_h, o_h, lse_h, causal, scale: float, chunks: int = 0,
+                        stream=None) -> None:
+    """fa_fwd_host without caller-owned device buffers, for callers that cannot allocate device
+    memory: the staging area is the library's fixed HOST_NOALLOC_MAX_BYTES device array, shared
+    by every call on the device (calls on different streams must not overlap in time).
+    q_h .. lse_h are contiguous CPU tensors (pinned for overlap); asynchronous on `stream`."""
+    for name, h in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h), ("o_h", o_h), ("lse_h", lse_h)):
+        if not isinstance(h, torch.Tensor) or h.is_cuda or not h.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    if q_h.dim() != 4 or k_h.dim() != 4 or k_h.shape != v_h.shape or o_h.shape != q_h.shape or \
+            tuple(lse_h.shape) != tuple(q_h.shape[:3]) or q_h.shape[0] != k_h.shape[0] or q_h.shape[3] != k_h.shape[3]:
+        raise ValueError("q_h, o_h [B,Hq,Sq,D], k_h, v_h [B,Hkv,Sk,D] and lse_h [B,Hq,Sq] expected")
+    if not (q_h.dtype == k_h.dtype == v_h.dtype == o_h.dtype) or q_h.dtype not in (torch.bfloat16, torch.float16) \
+            or lse_h.dtype != torch.float32:
+        raise ValueError("q_h, k_h, v_h, o_h share one 16-bit dtype; lse_h is float32")
+    B, Hq, Sq, D = q_h.shape
+    Hkv, Sk = k_h.shape[1], k_h.shape[2]
+    st = load_library().fa_fwd_host_noalloc(
+        q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
+        B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_h.dtype == torch.float16), int(chunks),
         _stream_handle(stream))
     if st != 0:
         raise FaError(st, fa_strerror(st))

@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 def sources():
     return [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "fa_fwd1_sm103.cu", "gemm_sm103.cu", "softmax_sm103.cu", "fa_api.cpp",
-                                                  "host_pipeline.cpp")]
+                                                  "host_pipeline.cpp", "host_noalloc.cu")]
 
 
 def _stale(path: str) -> bool:

@@ -299,6 +299,7 @@ const char *fa_strerror(int status)
     case FA_ERR_CAUSAL: return "FA_ERR_CAUSAL: causal must be 0 (none), 1 (top-left) or 2 (bottom-right)";
     case FA_ERR_SHAPE: return "FA_ERR_SHAPE: matrix rows must be 16-byte multiples (K and N multiples of 8)";
     case FA_ERR_ARG: return "FA_ERR_ARG: dtype, output type or epilogue selector out of range";
+    case FA_ERR_TOO_LARGE: return "FA_ERR_TOO_LARGE: the problem needs more staging than FA_HOST_NOALLOC_MAX_BYTES";
     default: return "unknown fa status code";
     }
 }

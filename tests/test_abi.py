@@ -47,7 +47,7 @@ def test_library_exports_every_declared_function(lib):
 
 def test_strerror_covers_every_code(lib):
     codes = declared_status_codes()
-    assert len(codes) == 16 and sorted(codes.values()) == list(range(16))
+    assert len(codes) == 17 and sorted(codes.values()) == list(range(17))
     msgs = set()
     for name, val in codes.items():
         msg = lib.fa_strerror(val).decode()
@@ -206,3 +206,40 @@ def test_host_entry_point_empty_and_shared_inputs(lib):
     # host inputs may share memory (they are only read): the call then gets as far as the
     # overlap checks of the written ranges, here a clash of lse_h with o_h
     assert call_host(lib, kh=QH, vh=QH, lh=OH) == 6
+
+
+# fa_fwd_host_noalloc(q_h, k_h, v_h, o_h, lse_h, sizes..., dtype, chunks, stream): the device
+# staging area is the library's own, so only host pointers are passed.
+def call_noalloc(lib, dtype=0, chunks=0, **over):
+    a = dict(GOOD, qh=QH, kh=KH, vh=VH, oh=OH, lh=LH)
+    a.update(over)
+    return lib.fa_fwd_host_noalloc(a["qh"], a["kh"], a["vh"], a["oh"], a["lh"], a["B"], a["Hq"], a["Hkv"],
+                                   a["Sq"], a["Sk"], a["D"], a["causal"], a["scale"], dtype, chunks, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), 15), (dict(chunks=-1), 15), (dict(chunks=65), 15),
+    (dict(D=96), 4), (dict(Hq=3), 3), (dict(causal=3), 13), (dict(scale=math.nan), 7), (dict(Sk=0), 2),
+    (dict(B=-1), 2), (dict(qh=None), 1), (dict(lh=None), 1),
+    (dict(oh=QH + 64), 6), (dict(lh=OH + 4), 6), (dict(lh=KH), 6),
+    # staging needs more than the 64 MiB area: q alone is 2 * 32 * 4096 * 128 * 2 B = 64 MiB
+    (dict(B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128), 16),
+    # 16-bit q, k, v, o at 4 * 16 * 1024 * 64 * 2 B = 8 MiB each + lse fits; eight times the keys does not
+    (dict(B=4, Hq=16, Hkv=16, Sq=1024, Sk=8192, D=64), 16),
+    # a key count whose byte product would overflow 64 bits is still only "too large"
+    (dict(B=1, Hq=1, Hkv=1, Sq=1, Sk=2**31 - 1, D=256), 16),
+])
+def test_noalloc_entry_point_rejects_before_any_cuda_call(lib, kw, code):
+    assert call_noalloc(lib, **kw) == code
+
+
+def test_noalloc_entry_point_empty_problems(lib):
+    assert call_noalloc(lib, B=0, qh=None, kh=None, vh=None, oh=None, lh=None) == 0
+    assert call_noalloc(lib, Sq=0) == 0
+
+
+def test_noalloc_capacity_matches_the_header():
+    from programming_flashattention_fwd_gb300 import binding
+    text = open(HEADER).read()
+    m = re.search(r"#define FA_HOST_NOALLOC_MAX_BYTES \((\d+)ull << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == binding.HOST_NOALLOC_MAX_BYTES
