@@ -561,28 +561,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const uint64_t il2 = f2_pack(inv_l, inv_l);
             uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)u.zq * p.Sq + row) * (size_t)(D * 2);
+            // Without a causal mask both tiles of a unit end on the same key step, so their
+            // epilogues run together with no other tile's work beside them: there O is read in
+            // one round trip (all D columns, one wait).  With the mask, tile b's extra diagonal
+            // step runs beside tile a's epilogue, and four shorter round trips measured faster.
+            constexpr int kChunk = CAUSAL ? 32 : D;
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t ov[32];
-                tmem_ld_x32(tO + c, ov);
+            for (int c0 = 0; c0 < D; c0 += kChunk) {
+                uint32_t ovc[kChunk];
+#pragma unroll
+                for (int c = 0; c < kChunk; c += 32)
+                    tmem_ld_x32(tO + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(ovc + c));
                 tmem_wait_ld();
-                reg_fence_x32(ov);
-                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float lo, hi;
-                    f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), il2), lo, hi);
-                    pk[e] = pack2<BF16>(lo, hi);
-                }
-                if (row < p.Sq) {
-                    if (p.o_al32) {   // full 32-byte sectors: half the store instructions, no partial sectors
-                        st_global_v8(orow + c * 2, pk);
-                        st_global_v8(orow + c * 2 + 32, pk + 8);
-                    } else {
+                for (int c = 0; c < kChunk; c += 32) reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(ovc + c));
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            st_global_v4(orow + c * 2 + q4 * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
-                                         pk[4 * q4 + 3]);
+                for (int c = c0; c < c0 + kChunk; c += 32) {
+                    const uint32_t *ov = ovc + (c - c0);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float lo, hi;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), il2),
+                                  lo, hi);
+                        pk[e] = pack2<BF16>(lo, hi);
+                    }
+                    if (row < p.Sq) {
+                        if (p.o_al32) {   // full 32-byte sectors: half the store instructions, no partial sectors
+                            st_global_v8(orow + c * 2, pk);
+                            st_global_v8(orow + c * 2 + 32, pk + 8);
+                        } else {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                st_global_v4(orow + c * 2 + q4 * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
+                                             pk[4 * q4 + 3]);
+                        }
                     }
                 }
             }
