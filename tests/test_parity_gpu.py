@@ -264,26 +264,29 @@ def test_canaries_untouched(fa):
 
 @pytest.mark.parametrize("kernel,D", [(1, 64), (1, 128), (2, 128), (2, 256), (3, 128)])
 @pytest.mark.parametrize("offset", [8, 16])
-def test_output_alignment_paths(fa, orc, kernel, D, offset):
+@pytest.mark.parametrize("causal", [0, 1])
+def test_output_alignment_paths(fa, orc, kernel, D, offset, causal):
     """o 32-byte aligned (rows written in 32-byte sectors) or only 16-byte aligned (16-byte
-    stores): same bits either way, and parity with the oracle; nothing written outside o."""
-    w = Workload("align", 1, 4, 2, 300, 260, D, "bf16", 1, 17 + D)
+    stores): same bits either way, and parity with the oracle; nothing written outside o.
+    Both masks, since the two-tile kernel reads O for its epilogue differently with and
+    without the causal mask."""
+    w = Workload("align", 1, 4, 2, 300, 260, D, "bf16", causal, 17 + D)
     q, k, v = make_qkv(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     n_o = q.numel()
     obuf = torch.full((n_o + 64,), 12345.0, dtype=torch.bfloat16, device="cuda")
     o = obuf[offset:offset + n_o].view(q.shape)       # 16 (offset 8) or 32 bytes (offset 16) from a 256-byte base
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
-    fa.fa_fwd_select(qd, kd, vd, o, lse, 1, w.softmax_scale, kernel)
+    fa.fa_fwd_select(qd, kd, vd, o, lse, causal, w.softmax_scale, kernel)
     o_al = torch.empty_like(qd)
     lse_al = torch.empty_like(lse)
-    fa.fa_fwd_select(qd, kd, vd, o_al, lse_al, 1, w.softmax_scale, kernel)
+    fa.fa_fwd_select(qd, kd, vd, o_al, lse_al, causal, w.softmax_scale, kernel)
     torch.cuda.synchronize()
     assert o.data_ptr() % 32 == (16 if offset == 8 else 0)
     assert torch.equal(o, o_al) and torch.equal(lse, lse_al)
     assert (obuf[:offset] == 12345.0).all() and (obuf[offset + n_o:] == 12345.0).all()
-    o_ref, l_ref = orc.full(q, k, v, False, 1, w.softmax_scale)
-    check(o, lse, o_ref, l_ref, f"kernel {kernel} D {D} offset {offset}")
+    o_ref, l_ref = orc.full(q, k, v, False, causal, w.softmax_scale)
+    check(o, lse, o_ref, l_ref, f"kernel {kernel} D {D} offset {offset} causal {causal}")
 
 
 def test_deterministic_and_side_stream(fa):
