@@ -62,8 +62,8 @@ PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
 # device headers and the host code that encodes its tensor maps and launch shape.
 COMMON_SOURCES = ("ptx.cuh", "watchdog.cuh", "fa_internal.h", "fa_api.cpp")
 KERNEL_SOURCES = {
-    "fa::fa_fwd_kernel": ("fa_fwd_sm103.cu",),
-    "fa::fa_fwd1_kernel": ("fa_fwd1_sm103.cu",),
+    "fa::fa_fwd_kernel": ("fa_fwd_sm103.cu", "schedule.h"),
+    "fa::fa_fwd1_kernel": ("fa_fwd1_sm103.cu", "schedule.h"),
     "fa::gemm::gemm_kernel": ("gemm_sm103.cu",),
     "fa::sm::softmax_regs_kernel": ("softmax_sm103.cu",),
 }

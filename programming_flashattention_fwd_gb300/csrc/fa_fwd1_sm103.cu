@@ -28,6 +28,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "schedule.h"
 #include "watchdog.cuh"
 
 namespace fa {
@@ -73,36 +74,13 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
 };
 
-struct Unit {
-    int zq, zkv, t, nk;
-};
+// One work unit, decoded identically by every role (the schedule is in schedule.h).
+using Unit = TileUnit;
 
 template <bool CAUSAL, int BN>
 __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
 {
-    const int G = gridDim.x, c = blockIdx.x;
-    const long long g = (long long)round * G + ((round & 1) ? (G - 1 - c) : c);
-    if (g >= p.num_units) return false;
-    int bh, t;
-    if (CAUSAL) {   // heaviest query tiles first
-        const int nbh = p.B * p.Hq;
-        t = p.Tq - 1 - (int)(g / nbh);
-        bh = (int)(g % nbh);
-    } else {
-        bh = (int)(g / p.Tq);
-        t = (int)(g % p.Tq);
-    }
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    u.zq = b * p.Hq + hq;
-    u.zkv = b * p.Hkv + hq / p.group;
-    u.t = t;
-    if (!CAUSAL) {
-        u.nk = p.Tk;
-    } else {
-        const long long hi = (long long)t * BM + (BM - 1) + p.coff;
-        u.nk = hi < 0 ? 0 : (int)min((long long)p.Tk, hi / BN + 1);
-    }
-    return true;
+    return tile_unit<CAUSAL, BN>(p, gridDim.x, blockIdx.x, round, u);
 }
 
 template <int D, int KEYS, bool BF16, bool CAUSAL>

@@ -44,6 +44,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace fa {
 
@@ -108,46 +109,13 @@ __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar)
                  : "memory");
 }
 
-// One work unit, decoded identically by every role.
-struct Unit {
-    int zq, zkv;      // q/o head plane (b*Hq + hq) and k/v head plane (b*Hkv + kvh)
-    int tA, tB;       // query tile indices
-    bool hasB;
-    int nA, nB, n;    // key tiles for tile a, tile b, and their maximum
-};
+// One work unit, decoded identically by every role (the schedule is in schedule.h).
+using Unit = PairUnit;
 
 template <bool CAUSAL>
 __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
 {
-    const int G = gridDim.x, c = blockIdx.x;
-    const long long g = (long long)round * G + ((round & 1) ? (G - 1 - c) : c);   // snake order
-    if (g >= p.num_units) return false;
-    int bh, pr;
-    if (CAUSAL) {   // heaviest query-tile pairs first
-        const int nbh = p.B * p.Hq;
-        pr = p.NP - 1 - (int)(g / nbh);
-        bh = (int)(g % nbh);
-    } else {        // consecutive units share a head (and its K/V in L2)
-        bh = (int)(g / p.NP);
-        pr = (int)(g % p.NP);
-    }
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    u.zq = b * p.Hq + hq;
-    u.zkv = b * p.Hkv + hq / p.group;
-    u.tA = 2 * pr;
-    u.tB = 2 * pr + 1;
-    u.hasB = u.tB < p.Tq;
-    // key tiles a query tile needs: causal -> up to the tile holding key (last row + coff);
-    // 0 when even its last row has no allowed key (bottom-right alignment with Sq > Sk)
-    auto key_tiles = [&](int t) {
-        if (!CAUSAL) return p.Tk;
-        const long long hi = (long long)t * kBM + (kBM - 1) + p.coff;
-        return hi < 0 ? 0 : (int)min((long long)p.Tk, hi / kBN + 1);
-    };
-    u.nA = key_tiles(u.tA);
-    u.nB = u.hasB ? key_tiles(u.tB) : 0;
-    u.n = max(u.nA, u.nB);
-    return true;
+    return pair_unit<CAUSAL>(p, gridDim.x, blockIdx.x, round, u);
 }
 
 template <int D, bool BF16, bool CAUSAL>
