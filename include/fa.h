@@ -126,7 +126,7 @@ int fa_device_status(fa_stream_t stream, uint32_t *detail);
  * expires; the kernel then records FA_ERR_DEVICE_TIMEOUT and every CTA returns normally),
  * the kernel variant (as fa_fwd_select) and the lazy-rescale threshold tau in log2 units
  * (O and l are rescaled only when the running row maximum grows by more than tau; 0 rescales
- * at every new maximum; negative = the default 8; above 15 -- where an unnormalised P could
+ * at every new maximum; negative = the default 12; above 15 -- where an unnormalised P could
  * leave the fp16 range -- or NaN returns FA_ERR_ARG).
  * With inject == 0, timeout_ns == 0, kernel == 0 and tau < 0 it is exactly fa_fwd / fa_fwd_fp16.
  */

@@ -163,7 +163,7 @@ def fa_fwd_fp16(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> Non
 def fa_fwd_debug(q, k, v, o, lse, causal: bool, scale: float, timeout_ns: int = 0,
                  inject: int = 0, kernel: int = 0, tau: float = -1.0, stream=None) -> None:
     """Test hook: the forward with an explicit watchdog limit, fault-injection mask, kernel
-    variant and lazy-rescale threshold tau (log2 units; negative = the default 8)."""
+    variant and lazy-rescale threshold tau (log2 units; negative = the default 12)."""
     _call("fa_fwd_debug", q, k, v, o, lse, causal, scale, stream,
           extra=(int(q.dtype == torch.float16), int(timeout_ns), int(inject), int(kernel), float(tau)))
 

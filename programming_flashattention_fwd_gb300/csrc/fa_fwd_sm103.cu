@@ -29,7 +29,7 @@
 //
 // Differences from the guide's kernel: exp2 with |scale|*log2(e) folded into one FMA; the
 // rescale of O is lazy (only when the running max grows by more than a factor 2^tau,
-// tau = 8 unless a test sets it, so the unnormalised P stays <= 256, well inside bf16/fp16
+// tau = 12 unless a test sets it, so the unnormalised P stays <= 4096, well inside bf16/fp16
 // range; O and l always share the same stale max, so the result is unchanged); a negative
 // scale negates S inside the MMA and a zero scale zeroes Q at load time; K/V tails and the causal diagonal are masked only
 // on the tiles that need it; fully masked causal tiles are skipped; the log-sum-exp is

@@ -207,16 +207,16 @@ def test_large_logit_rows(fa, orc, seed, causal):
 @pytest.mark.parametrize("kernel,D", [(1, 64), (1, 128), (2, 128), (3, 128), (2, 256)])
 def test_lazy_rescale_threshold(fa, orc, kernel, D):
     """The result does not depend on the lazy-rescale threshold: tau = 0 (rescale at every new
-    row maximum, the tutorial's recurrence), the default 8 and 15 (P up to 2^15 before a
+    row maximum, the tutorial's recurrence), 8, the default 12 and 15 (P up to 2^15 before a
     rescale, the most the fp16 range allows) each match the oracle, on large-logit inputs
-    whose row maxima keep growing across key tiles, and the three outputs agree with one
+    whose row maxima keep growing across key tiles, and the four outputs agree with one
     another to within the 16-bit rounding of O."""
     w = Workload("tau", 1, 4, 2, 300, 700, D, "fp16" if D == 64 else "bf16", 1, 31 + D + kernel,
                  q_std=2.0, k_std=2.0)
     q, k, v = make_qkv(w)
     o_ref, l_ref = orc.full(q, k, v, w.is_fp16, w.causal, w.softmax_scale)
     outs = []
-    for tau in (0.0, 8.0, 15.0):
+    for tau in (0.0, 8.0, 12.0, 15.0):
         qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
         o = torch.full_like(qd, float("nan"))
         lse = torch.full(qd.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
