@@ -70,9 +70,11 @@ extern "C" int fa_fwd_host_noalloc(const void *q_h, const void *k_h, const void 
     if (st != FA_ERR_NULL_PTR) return st;
     if (!q_h || !k_h || !v_h || !o_h || !lse_h) return FA_ERR_NULL_PTR;
 
-    // Staging bytes, first in double (the products cannot overflow there), then exactly.
-    const double need = 2.0 * ((double)B * Hq * Sq * D * 2 + kSliceAlign) +
-                        2.0 * ((double)B * Hkv * Sk * D * 2 + kSliceAlign) + ((double)B * Hq * Sq * 4 + kSliceAlign);
+    // Staging bytes.  First the unrounded total in double, where the products cannot overflow:
+    // it is a lower bound, so above the cap the problem is too large.  Below it every size fits
+    // in size_t, and the exact total with each slice rounded up decides.
+    const double need = 2.0 * ((double)B * Hq * Sq * D * 2) + 2.0 * ((double)B * Hkv * Sk * D * 2) +
+                        (double)B * Hq * Sq * 4;
     if (need > (double)kCap) return FA_ERR_TOO_LARGE;
     const size_t nq = (size_t)B * Hq * Sq * D * 2, nk = (size_t)B * Hkv * Sk * D * 2, nl = (size_t)B * Hq * Sq * 4;
     const size_t off_q = 0, off_k = off_q + round_up(nq), off_v = off_k + round_up(nk),

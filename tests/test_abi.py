@@ -243,3 +243,14 @@ def test_noalloc_capacity_matches_the_header():
     text = open(HEADER).read()
     m = re.search(r"#define FA_HOST_NOALLOC_MAX_BYTES \((\d+)ull << (\d+)\)", text)
     assert m and int(m.group(1)) << int(m.group(2)) == binding.HOST_NOALLOC_MAX_BYTES
+
+
+def test_noalloc_capacity_boundary(lib):
+    """The 64 MiB staging area holds q, k, v, o and lse, each rounded up to 256 bytes.  D = 64,
+    one head, Sq = 64: q and o take 8192 bytes each, lse 256, k and v 128 * Sk each.  Sk = 262078
+    needs 67108608 bytes (fits), Sk = 262080 needs 67109120 (does not).  Both calls pass o_h
+    overlapping q_h, so the one that fits stops at the overlap check, before any CUDA call."""
+    over = dict(B=1, Hq=1, Hkv=1, Sq=64, D=64, causal=0, oh=QH + 64)
+    assert 2 * 8192 + 256 + 2 * 128 * 262078 <= 64 << 20 < 2 * 8192 + 256 + 2 * 128 * 262080
+    assert call_noalloc(lib, Sk=262078, **over) == 6
+    assert call_noalloc(lib, Sk=262080, **over) == 16

@@ -88,3 +88,19 @@ def test_noalloc_matches_caller_staged_entry_point_on_two_calls_in_a_row(fa):
     assert fa.fa_device_status() == (0, 0)
     for (o, lse), (o_ref, l_ref) in zip(outs, refs):
         assert_close(o, lse, o_ref, l_ref)
+
+
+def test_noalloc_problem_filling_most_of_the_staging_area(fa):
+    """q, k, v, o and lse of this problem take 62.75 MiB of the 64 MiB area, so the slices run
+    up to its end; the result must still agree with the caller-staged entry point."""
+    w = Workload("noalloc_big", 1, 32, 32, 2000, 2000, 128, "bf16", 1, seed=9003)
+    need = 4 * (w.B * w.Hq * w.Sq * w.D * 2) + w.B * w.Hq * w.Sq * 4
+    assert need <= fa.HOST_NOALLOC_MAX_BYTES and need > 0.95 * fa.HOST_NOALLOC_MAX_BYTES
+    q, k, v = make_qkv(w)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_ref, l_ref = with_caller_staging(fa, w, qh, kh, vh)
+    s = torch.cuda.Stream()
+    o, lse = noalloc_c_abi(fa, w, qh, kh, vh, s)
+    s.synchronize()
+    assert fa.fa_device_status() == (0, 0)
+    assert_close(o, lse, o_ref, l_ref)
