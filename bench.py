@@ -1,9 +1,14 @@
 #!/usr/bin/env python3
 """Benchmark of the attention forward pass on GB300 -- one JSON line on stdout.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload suite|NAME] [--impl ours|reference]
 
 A step is one fa_fwd call over the whole workload (every query row of every head and batch).
+By default (``--workload suite``) the run times five workloads one after another: the largest
+one, B=1 Hq=32 Hkv=8 S=16384 D=128 bf16 causal, whose figures are the top level of the line,
+then the 4096-token GQA causal one, the non-causal fp16 one (S=2000, large logits), the D=64
+causal one and the smallest one; ``per_config`` holds each workload's value, step time,
+roofline (fractions of the burst and of the sustained peak), clocks and CPU-oracle baseline.
 ``value`` is attention TFLOP/s (4*B*Hq*Sq*Sk*D, halved when causal) over the K timed steps,
 timed with CUDA events on the launching stream with the inputs resident in HBM; the L2 is
 flushed (a 256 MiB write) between timed steps, outside the events.  ``e2e`` is the same
@@ -21,7 +26,8 @@ GB300s (MEASURED_PEAKS.json when present, else the fallback figure, as stated in
 query rows, on all host cores.
 
 ``--impl reference`` times that oracle instead (the reference arm: there is no other
-implementation of these pages to run): each step evaluates a bounded sample of query rows.
+implementation of these pages to run): each step evaluates a bounded sample of query rows of
+the headline workload.
 
 ``--op gemm | gemm_gelu | softmax`` measures the standalone building blocks instead of the
 attention call (same JSON fields): the tiled matrix product (bf16, M = N = K = 8192 by
@@ -55,6 +61,12 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 E2E_INFLIGHT_CHUNKS = 2      # fa_fwd_host pipeline depth per call when two calls are in flight
 PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
+# The default run: the largest single-GPU workload first (the headline of the line), then the
+# other benchmark workloads -- the 4096-token GQA causal one, the non-causal fp16 one with
+# large logits and a ragged tail, the D = 64 causal one and the smallest one.
+SUITE = ("gqa_causal_b1_h32kv8_s16384", "gqa_causal_b2_h32kv8_s4096", "mha_fp16_b8_h16_s2000_std2",
+         "mha_causal_b4_h16_s1024_d64", "mha_b1_h2_s128_d64")
+TARGET_FRAC = 0.60    # of the dense bf16 peak, stated for the D = 128 workloads
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -159,7 +171,6 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -178,31 +189,30 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def mark(self, which):
-        if which == "start":
-            self.t0 = time.time()
-        else:
-            self.t1 = time.time()
-
     def stop(self):
+        """Ends sampling; window() then summarises any interval of the run."""
         if self.proc is None:
-            return None
+            return
         time.sleep(0.12)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+
+    def window(self, t0, t1):
+        """Median SM clock, maximum clock and throttle reasons seen in [t0, t1] (or the samples
+        nearest to it when the interval is shorter than the sampling period)."""
         rows = []
         for ts, line in self.lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 10:
                 continue
             rows.append((ts, parts))
-        inside = [r for r in rows if self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        inside = [r for r in rows if t0 - 0.06 <= r[0] <= t1 + 0.06]
         where = "during timed region"
         if not inside and rows:
-            inside = sorted(rows, key=lambda r: abs(r[0] - self.t1))[:3]
+            inside = sorted(rows, key=lambda r: abs(r[0] - t1))[:3]
             where = "nearest samples to the timed region (region shorter than the sampling period)"
         if not inside:
             return None
@@ -328,24 +338,21 @@ def workload_config(w, args):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_ours(args, w, world, rank, local):
+def time_device(args, w, world, rank, dev, fn):
+    """Device-timed calls of `fn` on workload `w` (inputs resident in HBM): W warm-up calls, then K
+    calls each bracketed by CUDA events on the launching stream with a 256 MiB L2 flush between
+    them (outside the events), then up to 50 calls back to back (warm L2, for reference).
+    Returns the timing record and the host/device tensors for the end-to-end leg."""
     import numpy as np
     import torch
     from programming_flashattention_fwd_gb300 import binding
     from programming_flashattention_fwd_gb300.inputs import make_qkv
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    binding.load_library()
     wr = w.with_(seed=w.seed + 7919 * rank) if rank else w     # independent replica per rank
     q_h, k_h, v_h = make_qkv(wr)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    if args.kernel:
-        fn = lambda q_, k_, v_, o_, l_, c_, s_: binding.fa_fwd_select(q_, k_, v_, o_, l_, c_, s_, args.kernel)
-    else:
-        fn = binding.fa_fwd_fp16 if w.is_fp16 else binding.fa_fwd
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -354,34 +361,28 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.synchronize(dev)
     st, word = binding.fa_device_status()
     if st != 0:
-        raise RuntimeError(f"device watchdog fired during warm-up (word {word:#x})")
+        raise RuntimeError(f"device watchdog fired during warm-up of {w.name} (word {word:#x})")
 
-    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
-    if sampler:
-        sampler.start()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark("start")
+    t0 = time.time()
     for s in range(args.steps):
         flush.zero_()
         starts[s].record(stream)
         fn(q, k, v, o, lse, w.causal, w.softmax_scale)
         ends[s].record(stream)
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark("end")
+    t1 = time.time()
     barrier(world)
-    clocks = sampler.stop() if sampler else None
     times = [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
     t_step = max_over_ranks(sum(times) / len(times), world)
     st, word = binding.fa_device_status()
     if st != 0:
-        raise RuntimeError(f"device watchdog fired during the timed steps (word {word:#x})")
+        raise RuntimeError(f"device watchdog fired during the timed steps of {w.name} (word {word:#x})")
 
-    # ---- the same calls back to back without the L2 flush (warm L2), for reference only
+    # the same calls back to back without the L2 flush (warm L2), for reference only
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_warm = min(args.steps, 50)
     w0.record(stream)
@@ -390,8 +391,44 @@ def run_ours(args, w, world, rank, local):
     w1.record(stream)
     torch.cuda.synchronize(dev)
     t_warm = max_over_ranks(w0.elapsed_time(w1) * 1e-3 / n_warm, world)
+    rec = {"t_step": t_step, "times": times, "t_warm": t_warm, "n_warm": n_warm, "window": (t0, t1)}
+    return rec, (q_h, k_h, v_h), (q, k, v, o, lse)
 
-    # ---- end to end through the public binding, pinned host buffers, copies inside the events
+
+def roofline_record(w, args, t_step):
+    """Achieved TFLOP/s of the attention kernel against the measured dense bf16 peaks: `frac` is
+    of the burst figure (the kernel is timed alone), `frac_sustained` of the sustained one."""
+    peak, peak_sus, peak_src = measured_peaks()
+    achieved = w.flops() / t_step / 1e12
+    kname = attention_kernel(w, args.kernel)
+    rec = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+           "frac": achieved / peak, "traffic": ncu_traffic(w.name, kname),
+           "peak_source": f"{peak_src} dense bf16 (burst)" + (f"; sustained {peak_sus}" if peak_sus else ""),
+           "kernel": kname}
+    if peak_sus:
+        rec["peak_sustained"] = peak_sus
+        rec["frac_sustained"] = achieved / peak_sus
+    return rec
+
+
+def timing_record(rec, w, world):
+    import numpy as np
+    times, t_warm = rec["times"], rec["t_warm"]
+    return {"ms_mean": rec["t_step"] * 1e3, "ms_median": float(np.median(times)) * 1e3,
+            "ms_min": min(times) * 1e3, "ms_max": max(times) * 1e3,
+            "warm_l2_ms_per_step": t_warm * 1e3, "warm_l2_value": w.flops() * world / t_warm / 1e12,
+            "note": "value uses ms_mean over L2-flushed calls (rank max); the warm figure times "
+                    f"{rec['n_warm']} calls back to back without the flush"}
+
+
+def time_e2e(args, w, world, dev, fn, host, devt):
+    """End to end through the host-memory entry point (fa_fwd_host): pinned host q, k, v in,
+    o and lse back, copies inside the events; two calls in flight and one at a time."""
+    import torch
+    from programming_flashattention_fwd_gb300 import binding
+    q_h, k_h, v_h = host
+    q, k, v, o, lse = devt
+    stream = torch.cuda.current_stream(dev)
     q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     o_p = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
     l_p = torch.empty(q_h.shape[:3], dtype=torch.float32).pin_memory()
@@ -401,7 +438,7 @@ def run_ours(args, w, world, rank, local):
 
     # pipeline depth of fa_fwd_host: one call at a time takes the library's default (4 chunks);
     # with two calls in flight the neighbouring call already fills the link, and 2 chunks per
-    # call measured best (456 against 430 TFLOP/s with 4 on the 4096-token default)
+    # call measured best (456 against 430 TFLOP/s with 4 on the 4096-token workload)
     chunks_serial = args.chunks
     chunks_inflight = args.chunks if args.chunks else E2E_INFLIGHT_CHUNKS
 
@@ -461,41 +498,79 @@ def run_ours(args, w, world, rank, local):
         assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu()), "e2e result differs from the device run"
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * q_h.element_size()
     d2h = o_p.numel() * o_p.element_size() + l_p.numel() * 4
+    flops = w.flops()
+    return {"value": flops * world / t_e2e / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+            "calls_in_flight": 2, "chunks_per_call": chunks_inflight or 4,
+            "serial_chunks_per_call": chunks_serial or 4, "serial_ms_per_step": t_serial * 1e3,
+            "serial_value": flops * world / t_serial / 1e12,
+            "api": "fa_fwd_host" if not args.kernel else "torch copies + fa_fwd_select"}
 
+
+def run_ours(args, workloads, world, rank, local):
+    """Times every workload in `workloads` on the device; the first is the headline of the JSON
+    line (its value, config, roofline, e2e and cpu_baseline at the top level) and every one,
+    the headline included, gets an entry in `per_config`."""
+    import torch
+    from programming_flashattention_fwd_gb300 import binding
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
+    if sampler:
+        sampler.start()
+
+    results = []
+    e2e = None
+    for i, w in enumerate(workloads):
+        if args.kernel:
+            fn = lambda q_, k_, v_, o_, l_, c_, s_: binding.fa_fwd_select(q_, k_, v_, o_, l_, c_, s_, args.kernel)
+        else:
+            fn = binding.fa_fwd_fp16 if w.is_fp16 else binding.fa_fwd
+        rec, host, devt = time_device(args, w, world, rank, dev, fn)
+        if i == 0:
+            e2e = time_e2e(args, w, world, dev, fn, host, devt)
+        results.append((w, rec, host))
+        del devt
+        torch.cuda.empty_cache()
+    if sampler:
+        sampler.stop()
+        time.sleep(0.05)
     if rank != 0:
         return
-    flops = w.flops()
-    peak, peak_sus, peak_src = measured_peaks()
-    achieved = flops / t_step / 1e12
-    kname = attention_kernel(w, args.kernel)
-    traffic = ncu_traffic(w.name, kname)
+
+    per_config = {}
+    for i, (w, rec, host) in enumerate(results):
+        rec["clocks"] = sampler.window(*rec["window"]) if sampler else None
+        entry = {"value": w.flops() * world / rec["t_step"] / 1e12, "unit": UNIT,
+                 "ms_per_step": rec["t_step"] * 1e3, "config": workload_config(w, args),
+                 "roofline": roofline_record(w, args, rec["t_step"]), "clocks": rec["clocks"],
+                 "timing": timing_record(rec, w, world), "gpu_launches": args.steps,
+                 "target_frac": TARGET_FRAC if w.D == 128 else None}
+        if not args.no_cpu_baseline:
+            budget = args.cpu_seconds if i == 0 else args.cpu_seconds_per_config
+            entry["cpu_baseline"] = time_oracle(w, *host, budget, seed=w.seed + 100)
+        per_config[w.name] = entry
+
+    w, rec, _ = results[0]
+    head = per_config[w.name]
     line = {
-        "metric": METRIC, "value": flops * world / t_step / 1e12, "unit": UNIT,
+        "metric": METRIC, "value": head["value"], "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w, args),
-        "e2e": {"value": flops * world / t_e2e / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
-                "calls_in_flight": 2, "chunks_per_call": chunks_inflight or 4,
-                "serial_chunks_per_call": chunks_serial or 4, "serial_ms_per_step": t_serial * 1e3,
-                "serial_value": flops * world / t_serial / 1e12,
-                "api": "fa_fwd_host" if not args.kernel else "torch copies + fa_fwd_select"},
+        "config": head["config"],
+        "e2e": e2e,
         "gpu_launches": args.steps,
-        "timing": {"ms_mean": t_step * 1e3, "ms_median": float(np.median(times)) * 1e3,
-                   "ms_min": min(times) * 1e3, "ms_max": max(times) * 1e3,
-                   "warm_l2_ms_per_step": t_warm * 1e3, "warm_l2_value": flops * world / t_warm / 1e12,
-                   "note": "value uses ms_mean over L2-flushed calls (rank max); the warm figure times "
-                           f"{n_warm} calls back to back without the flush"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} dense bf16 (burst)" + (
-                         f"; sustained {peak_sus}" if peak_sus else ""),
-                     "kernel": kname},
-        "clocks": clocks,
+        "timing": head["timing"],
+        "roofline": head["roofline"],
+        "clocks": head["clocks"],
     }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = time_oracle(w, q_h, k_h, v_h, args.cpu_seconds, seed=w.seed + 100)
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if len(results) > 1:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
 
 
@@ -554,18 +629,19 @@ def run_op(args, world, rank, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark("start")
+    t_start = time.time()
     for s_ in range(args.steps):
         flush.zero_()
         starts[s_].record(stream)
         call()
         ends[s_].record(stream)
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark("end")
+    t_end = time.time()
     barrier(world)
-    clocks = sampler.stop() if sampler else None
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.window(t_start, t_end)
     t_step = max_over_ranks(sum(a_.elapsed_time(b_) * 1e-3 for a_, b_ in zip(starts, ends)) / args.steps, world)
     st, word = binding.fa_device_status()
     if st != 0:
@@ -649,14 +725,18 @@ def run_op(args, world, rank, local):
 
 
 def main():
-    from programming_flashattention_fwd_gb300.inputs import ALL_WORKLOADS as WORKLOADS, DEFAULT_BENCH_WORKLOAD
+    from programming_flashattention_fwd_gb300.inputs import ALL_WORKLOADS as WORKLOADS
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_BENCH_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="suite", choices=["suite"] + sorted(WORKLOADS),
+                    help="one workload, or 'suite': the headline (the largest, 16384-token GQA causal) "
+                         "followed by the other four benchmark workloads, each in per_config")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget (headline)")
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=4.0,
+                    help="oracle CPU-baseline budget of each other workload of the suite")
     ap.add_argument("--ref-seconds", type=float, default=90.0, help="reference-arm total budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -676,7 +756,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = WORKLOADS[args.workload]
+    names = SUITE if args.workload == "suite" else (args.workload,)
+    workloads = [WORKLOADS[n] for n in names]
+    w = workloads[0]
     world, rank, local = dist_init()
     if world != args.gpus and world > 1:
         args.gpus = world
@@ -689,7 +771,7 @@ def main():
     elif args.impl == "reference":
         run_reference(args, w, world, rank)
     else:
-        run_ours(args, w, world, rank, local)
+        run_ours(args, workloads, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

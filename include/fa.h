@@ -84,7 +84,6 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
            fa_stream_t stream);
 
-/* fa_fwd_fp16 -- identical to fa_fwd with IEEE fp16 q, k, v and o. */
 /*
  * fa_fwd_select -- fa_fwd (dtype 0, bf16) / fa_fwd_fp16 (dtype 1) with an explicit kernel
  * variant, for tuning sweeps (the course's lesson 10: a search space of meta-parameters
@@ -102,6 +101,7 @@ int fa_fwd_select(const void *q, const void *k, const void *v, void *o, float *l
                   int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                   fa_stream_t stream, int dtype, int kernel);
 
+/* fa_fwd_fp16 -- identical to fa_fwd with IEEE fp16 q, k, v and o. */
 int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                 fa_stream_t stream);
@@ -217,7 +217,9 @@ int fa_softmax_rows(const void *x, void *y, int rows, int cols, int dtype, fa_st
  * FA_ERR_TOO_LARGE.  That check and every argument check are made before any CUDA call.
  * The first call on a device (with that device current) looks up the array's device address
  * once (cudaGetSymbolAddress) and keeps it: make that first call before any stream capture
- * starts.  A failed look-up returns FA_ERR_NO_DEVICE.
+ * starts.  A failed look-up returns FA_ERR_NO_DEVICE.  The kept address belongs to the device's
+ * primary context as it was at that first call: do not call this entry point again on a device
+ * after cudaDeviceReset() (or any other reset of its primary context) in the same process.
  * Every call on a device shares the one array, and a call leaves its inputs and results
  * there.  Nothing in it has to start at zero: each call writes every byte it reads.  Calls
  * that run at the same time on the GPU race on the array: two calls on one stream run in

@@ -107,6 +107,26 @@ def _stream_handle(stream) -> int:
     return int(stream)
 
 
+def _check_stream_device(stream, device: torch.device) -> None:
+    """A torch.cuda.Stream passed with tensors must belong to their device: the library
+    enqueues on the stream but encodes and launches on the current device."""
+    if isinstance(stream, torch.cuda.Stream) and stream.device != device:
+        raise ValueError(f"stream is on {stream.device} but the tensors are on {device}")
+
+
+def _check_same_device(tensors) -> Optional[torch.device]:
+    """All non-empty CUDA tensors on one device; returns it (None if every tensor is empty)."""
+    dev = None
+    for name, t in tensors:
+        if t.numel() and t.is_cuda:
+            if dev is None:
+                dev = t.device
+            elif t.device != dev:
+                raise ValueError(f"{name} is on {t.device} but another tensor is on {dev}: "
+                                 "every tensor of one call must be on the same GPU")
+    return dev
+
+
 def _check_tensors(q, k, v, o, lse):
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
         if not isinstance(t, torch.Tensor):
@@ -115,6 +135,7 @@ def _check_tensors(q, k, v, o, lse):
             raise ValueError(f"{name} must be contiguous ([B, H, S, D] dense layout)")
         if t.numel() and not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
+    _check_same_device((("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)))
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or o.dim() != 4 or lse.dim() != 3:
         raise ValueError("q, k, v, o must be 4-D [B, H, S, D] and lse 3-D [B, Hq, Sq]")
     if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
@@ -134,14 +155,41 @@ def _causal_code(causal) -> int:
     return int(causal)
 
 
+class _OnDevice:
+    """Makes `device` current for the library call when it is not already (the C ABI works on
+    the current device); a no-op otherwise, so the common call pays nothing."""
+    __slots__ = ("idx", "prev")
+
+    def __init__(self, device: Optional[torch.device]):
+        self.idx = device.index if device is not None and device.type == "cuda" else None
+        self.prev = None
+
+    def __enter__(self):
+        if self.idx is not None:
+            cur = _cur_device() if _cur_device is not None else torch.cuda.current_device()
+            if cur != self.idx:
+                self.prev = cur
+                torch.cuda.set_device(self.idx)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
+
+
 def _call(fn_name: str, q, k, v, o, lse, causal: bool, scale: float, stream, extra=()):
     _check_tensors(q, k, v, o, lse)
+    dev = q.device if q.is_cuda else None
+    if dev is not None:
+        _check_stream_device(stream, dev)
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     lib = load_library()
-    st = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale),
-                               _stream_handle(stream), *extra)
+    with _OnDevice(dev):
+        st = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale),
+                                   _stream_handle(stream), *extra)
     if st != 0:
         raise FaError(st, fa_strerror(st))
 
@@ -190,11 +238,15 @@ def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, causal, sc
             raise ValueError(f"{name} must match its device buffer's shape and dtype")
     B, Hq, Sq, D = q_d.shape
     Hkv, Sk = k_d.shape[1], k_d.shape[2]
-    st = load_library().fa_fwd_host(
-        q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
-        q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(), lse_d.data_ptr(),
-        B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_d.dtype == torch.float16), int(chunks),
-        _stream_handle(stream))
+    dev = q_d.device if q_d.is_cuda else None
+    if dev is not None:
+        _check_stream_device(stream, dev)
+    with _OnDevice(dev):
+        st = load_library().fa_fwd_host(
+            q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
+            q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(), lse_d.data_ptr(),
+            B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_d.dtype == torch.float16), int(chunks),
+            _stream_handle(stream))
     if st != 0:
         raise FaError(st, fa_strerror(st))
 
@@ -216,10 +268,13 @@ def fa_fwd_host_noalloc(q_h, k_h, v_h, o_h, lse_h, causal, scale: float, chunks:
         raise ValueError("q_h, k_h, v_h, o_h share one 16-bit dtype; lse_h is float32")
     B, Hq, Sq, D = q_h.shape
     Hkv, Sk = k_h.shape[1], k_h.shape[2]
-    st = load_library().fa_fwd_host_noalloc(
-        q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
-        B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_h.dtype == torch.float16), int(chunks),
-        _stream_handle(stream))
+    # the staging area is taken on the current device: with a stream given, that is its device
+    dev = stream.device if isinstance(stream, torch.cuda.Stream) else None
+    with _OnDevice(dev):
+        st = load_library().fa_fwd_host_noalloc(
+            q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr(),
+            B, Hq, Hkv, Sq, Sk, D, _causal_code(causal), float(scale), int(q_h.dtype == torch.float16), int(chunks),
+            _stream_handle(stream))
     if st != 0:
         raise FaError(st, fa_strerror(st))
 
@@ -257,15 +312,21 @@ def gemm(a, b, bias=None, epilogue: int = 0, out_fp32: bool = False, c=None, str
     for name, t in (("a", a), ("b", b)):
         if not (t.is_cuda and t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if a.device != b.device:
+        raise ValueError(f"a is on {a.device} but b is on {b.device}")
+    _check_stream_device(stream, a.device)
     M, K = a.shape
     N = b.shape[1]
     if c is None:
         c = torch.empty((M, N), dtype=torch.float32 if out_fp32 else a.dtype, device=a.device)
     if epilogue and (bias is None or bias.dtype != torch.float32 or bias.numel() != N or not bias.is_cuda):
         raise ValueError("epilogues 1 and 2 need a float32 CUDA bias of N entries")
-    st = load_library().fa_gemm(a.data_ptr(), b.data_ptr(), c.data_ptr(), bias.data_ptr() if epilogue else None,
-                                M, N, K, 0 if a.dtype == torch.bfloat16 else 1, int(bool(out_fp32)), int(epilogue),
-                                _stream_handle(stream))
+    if c.device != a.device or (epilogue and bias.device != a.device):
+        raise ValueError("c and bias must be on a's device")
+    with _OnDevice(a.device):
+        st = load_library().fa_gemm(a.data_ptr(), b.data_ptr(), c.data_ptr(), bias.data_ptr() if epilogue else None,
+                                    M, N, K, 0 if a.dtype == torch.bfloat16 else 1, int(bool(out_fp32)),
+                                    int(epilogue), _stream_handle(stream))
     if st != 0:
         raise FaError(st, fa_strerror(st))
     return c
@@ -278,10 +339,12 @@ def softmax_rows(x, y=None, stream=None):
         raise ValueError("x must be a contiguous 2-D float32 or bf16 CUDA tensor")
     if y is None:
         y = torch.empty_like(x)
-    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous():
-        raise ValueError("y must match x")
-    st = load_library().fa_softmax_rows(x.data_ptr(), y.data_ptr(), x.shape[0], x.shape[1],
-                                        0 if x.dtype == torch.float32 else 1, _stream_handle(stream))
+    if y.shape != x.shape or y.dtype != x.dtype or not y.is_contiguous() or y.device != x.device:
+        raise ValueError("y must match x (shape, dtype, device)")
+    _check_stream_device(stream, x.device)
+    with _OnDevice(x.device):
+        st = load_library().fa_softmax_rows(x.data_ptr(), y.data_ptr(), x.shape[0], x.shape[1],
+                                            0 if x.dtype == torch.float32 else 1, _stream_handle(stream))
     if st != 0:
         raise FaError(st, fa_strerror(st))
     return y

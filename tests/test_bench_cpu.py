@@ -38,13 +38,29 @@ def test_attention_kernel_choice_follows_head_dim():
     assert bench.attention_kernel(w128, 3) == "fa::fa_fwd1_kernel"
 
 
-def test_committed_profiles_match_the_current_sources():
-    # every committed ncu summary names a kernel and workload, and its recorded traffic is
-    # picked up by the benchmark for the sources as they stand
+def test_committed_profiles_name_kernel_workload_and_source():
+    # every committed ncu summary names a kernel, a workload and the hash of the sources it
+    # measured; the benchmark reports its traffic only while that hash matches the sources
     import glob
     import re
+    from programming_flashattention_fwd_gb300.inputs import ALL_WORKLOADS
     for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         txt = open(path).read()
         kernel = re.search(r"^kernel: (\S+)$", txt, re.M).group(1)
         workload = re.search(r"^workload: (\S+)$", txt, re.M).group(1)
-        assert bench.ncu_traffic(workload, kernel) is not None, f"{path}: stale kernel_source_sha"
+        sha = re.search(r"^kernel_source_sha: ([0-9a-f]{16})$", txt, re.M).group(1)
+        assert kernel in bench.KERNEL_SOURCES, path
+        assert re.search(r"^traffic_bytes_per_launch: \d+", txt, re.M), path
+        if kernel.startswith("fa::fa_fwd"):
+            assert workload in ALL_WORKLOADS, path
+        fresh = sha == bench.kernel_source_hash(kernel)
+        assert (bench.ncu_traffic(workload, kernel) is not None) == fresh, path
+
+
+def test_suite_leads_with_the_largest_workload():
+    from programming_flashattention_fwd_gb300.inputs import WORKLOADS
+    assert set(bench.SUITE) == set(WORKLOADS)
+    head = WORKLOADS[bench.SUITE[0]]
+    assert head.flops() == max(w.flops() for w in WORKLOADS.values())
+    # the metric's non-causal half is in the suite
+    assert any(not WORKLOADS[n].causal and WORKLOADS[n].D == 128 for n in bench.SUITE)

@@ -2,10 +2,12 @@
 device memory (its staging area is a fixed device array inside the library).
 
 Two calls in a row, on different inputs, shapes and types, go through the C ABI of the new
-entry point; each result must agree with fa_fwd_host -- the entry point with caller-allocated
-device staging buffers -- within the parity tolerances (max |dO| <= 2e-2, mean |dO| <= 2e-3,
-max |dLSE| <= 1e-3).  The second call reuses the staging area the first call left filled, so
-a result that leaned on stale or zeroed staging would show there.
+entry point; each result must be bit-identical to fa_fwd_host's -- the entry point with
+caller-allocated device staging buffers -- since the same kernels run on the same values (the
+parity tolerances, max |dO| <= 2e-2, mean |dO| <= 2e-3, max |dLSE| <= 1e-3, are checked as
+well, so that a failure says how far off it is).  The second call reuses the staging area the
+first call left filled, so a result that leaned on stale or zeroed staging would show there,
+and so would staging slices that overlap.
 
 The file name sorts last so that a run stopping at the first failure has run every other test
 first; the test also passes alone in a fresh process.
@@ -63,6 +65,7 @@ def noalloc_c_abi(fa, w, qh, kh, vh, stream):
 
 
 def assert_close(o, lse, o_ref, l_ref):
+    """Within the parity tolerances, then bit for bit (the header promises identical results)."""
     d = (o.double() - o_ref.double()).abs().numpy()
     assert np.isfinite(d).all(), "o has non-finite entries where the reference has none"
     assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, (d.max(), d.mean())
@@ -70,6 +73,8 @@ def assert_close(o, lse, o_ref, l_ref):
     fin = np.isfinite(lr)
     assert np.array_equal(fin, np.isfinite(l))
     assert np.abs(l[fin] - lr[fin]).max(initial=0.0) <= LSE_ABS
+    assert torch.equal(o, o_ref), "o differs from fa_fwd_host's in some bits"
+    assert torch.equal(lse, l_ref), "lse differs from fa_fwd_host's in some bits"
 
 
 def test_noalloc_matches_caller_staged_entry_point_on_two_calls_in_a_row(fa):
