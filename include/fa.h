@@ -33,7 +33,7 @@
  * Asynchrony: the kernel is enqueued on `stream` (0 = the legacy default stream) and the
  * call returns without synchronising.  Argument errors are returned before any CUDA call
  * is made.  The call never aborts, exits or traps; a device-side watchdog failure is
- * reported later through fa_device_status().
+ * reported later through fa_device_status() and leaves NaN in the affected rows of o and lse.
  *
  * Thread safety: calls may be made from several host threads; the only shared mutable
  * state is the per-device watchdog status word and read-only caches of device properties.
@@ -112,8 +112,13 @@ const char *fa_strerror(int status);
 /*
  * fa_device_status -- synchronises `stream`, then reads and clears the current device's
  * watchdog word.  Returns FA_OK if no kernel since the last read gave up on a wait,
- * FA_ERR_DEVICE_TIMEOUT if one did (its CTAs then skipped the rest of their work and the
- * outputs of that call are unspecified), or FA_ERR_NO_DEVICE on a CUDA error.
+ * FA_ERR_DEVICE_TIMEOUT if one did, or FA_ERR_NO_DEVICE on a CUDA error.  A wait gives up
+ * only after its limit (2 s by default) without progress, e.g. when the GPU is preempted for
+ * that long.  The attention kernels then leave the call's outputs visibly invalid: every
+ * query row of every CTA that gave up holds NaN in o and in lse (rows of other CTAs hold
+ * their results), so a caller that does not poll this word still sees NaN, never a stale or
+ * partial value that looks like a result.  (fa_gemm and fa_softmax_rows outputs of such a
+ * call are unspecified.)
  * *detail (if non-NULL) receives the raw word: bit 0 = timeout, bits 8..15 = the wait
  * site that expired first.
  */

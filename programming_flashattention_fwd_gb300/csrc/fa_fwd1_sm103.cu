@@ -22,7 +22,8 @@
 //
 // The softmax consumes every P V completion in order: before publishing P(j) it waits for
 // P V(j-1) (already done in the steady state), so O can be rescaled safely; the epilogue waits
-// for the last one.  Every wait is bounded, as in the main kernel.
+// for the last one.  Every wait is bounded, as in the main kernel; a CTA that gives up writes
+// NaN into o and lse of every query row it was given.
 #include <atomic>
 #include <cstdint>
 
@@ -76,6 +77,17 @@ struct Cfg {
 
 // One work unit, decoded identically by every role (the schedule is in schedule.h).
 using Unit = TileUnit;
+
+// NaN (all-ones: NaN in bf16, fp16 and fp32) into query row `row` of head plane zq of o and lse.
+template <int D>
+__device__ __forceinline__ void poison_row(const Params &p, int zq, int row)
+{
+    if (row >= p.Sq) return;
+    uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)zq * p.Sq + row) * (size_t)(D * 2);
+#pragma unroll 1
+    for (int c = 0; c < D * 2; c += 16) st_global_v4(orow + c, ~0u, ~0u, ~0u, ~0u);
+    p.lse[(size_t)zq * p.Sq + row] = __uint_as_float(~0u);
+}
 
 template <bool CAUSAL, int BN>
 __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
@@ -144,6 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int use = 0;
             int skip = -1;   // fault injection (inject bit 0): the first V tile is never loaded
+            const uint64_t keep = l2_policy_evict_last();   // K/V tiles are read again by other tiles
             bool ok = true;
             auto load = [&](const CUtensorMap *m, int j, int zkv) {
                 const int s = use % C::NS;
@@ -156,7 +169,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive_expect_tx(bar_full(s), C::KVTILE);
 #pragma unroll
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d(sRing + s * C::KVTILE + pn * C::KVPANEL, m, pn * 64, j * BN, zkv, bar_full(s));
+                    tma_load_3d_hint(sRing + s * C::KVTILE + pn * C::KVPANEL, m, pn * 64, j * BN, zkv, bar_full(s),
+                                     keep);
                 ++use;
                 return true;
             };
@@ -177,6 +191,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ Q producer
         if (lane == 0) {
             int tau = 0;
+            const uint64_t once = l2_policy_evict_first();   // each query tile is read once
             bool ok = true;
             Unit u;
             for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
@@ -191,7 +206,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int zq = p.smode == 2 ? p.B * p.Hq : u.zq;
 #pragma unroll
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_3d(sQ + buf * C::QTILE + pn * C::QPANEL, &tmQ, pn * 64, u.t * BM, zq, bar_q(buf));
+                    tma_load_3d_hint(sQ + buf * C::QTILE + pn * C::QPANEL, &tmQ, pn * 64, u.t * BM, zq, bar_q(buf),
+                                     once);
                 ++tau;
             }
             for (int x = max(0, tau - C::NQ); x < tau; ++x)
@@ -438,6 +454,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
+    } else if (warp >= 4 && *abort_flag) {
+        // This CTA gave up on a wait: every row of every tile it was given gets NaN in o and lse
+        // (all roles have stopped), so that none of them keeps a value that looks valid.
+        const int r = threadIdx.x - 128;
+        Unit u;
+        for (int round = 0; unit_at<CAUSAL, C::BN>(p, round, u); ++round) poison_row<D>(p, u.zq, u.t * BM + r);
     }
 }
 

@@ -36,7 +36,9 @@
 // written out; output rows go out in full 32-byte sectors when o is 32-byte aligned.
 //
 // Every wait is bounded (watchdog): on expiry the kernel records a status word, raises a
-// CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM and returns.
+// CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM, writes NaN into o and lse
+// of every query row the CTA was responsible for (so that no row of an abandoned call keeps a
+// value that looks valid) and returns.
 #include <atomic>
 #include <cfloat>
 #include <climits>
@@ -107,6 +109,17 @@ __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar)
     asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
                  "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
                  : "memory");
+}
+
+// NaN (all-ones: NaN in bf16, fp16 and fp32) into query row `row` of head plane zq of o and lse.
+template <int D>
+__device__ __forceinline__ void poison_row(const Params &p, int zq, int row)
+{
+    if (row >= p.Sq) return;
+    uint8_t *orow = static_cast<uint8_t *>(p.o) + ((size_t)zq * p.Sq + row) * (size_t)(D * 2);
+#pragma unroll 1
+    for (int c = 0; c < D * 2; c += 16) st_global_v4(orow + c, ~0u, ~0u, ~0u, ~0u);
+    p.lse[(size_t)zq * p.Sq + row] = __uint_as_float(~0u);
 }
 
 // One work unit, decoded identically by every role (the schedule is in schedule.h).
@@ -185,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0 && lane == 0) {
             // ======================================================== K/V producer
             const int skip = (p.inject & 1u) ? 1 : -1;   // ring use 1 = the first V tile
+            const uint64_t keep = l2_policy_evict_last(); // K/V tiles are read again by other tiles
             int use = 0;                                  // ring uses armed so far
             bool ok = true;
             Unit u;
@@ -201,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const CUtensorMap *m = kv ? &tmV : &tmK;
 #pragma unroll
                         for (int pn = 0; pn < C::PANELS; ++pn)
-                            tma_load_3d(sRing + s * C::TILE + pn * C::PANEL, m, pn * 64, j * kBN, u.zkv,
-                                        bar_full(s));
+                            tma_load_3d_hint(sRing + s * C::TILE + pn * C::PANEL, m, pn * 64, j * kBN, u.zkv,
+                                             bar_full(s), keep);
                     }
                 }
             }
@@ -212,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 2 && lane == 0) {
             // ======================================================== Q producer
             int tau = 0;   // query tiles loaded so far (buffer tau % 3)
+            const uint64_t once = l2_policy_evict_first();   // each query tile is read once
             bool ok = true;
             Unit u;
             for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
@@ -230,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int zq = p.smode == 2 ? p.B * p.Hq : u.zq;
 #pragma unroll
                     for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d(sQ + buf * C::TILE + pn * C::PANEL, &tmQ, pn * 64, t * kBM, zq, bar_q(buf));
+                        tma_load_3d_hint(sQ + buf * C::TILE + pn * C::PANEL, &tmQ, pn * 64, t * kBM, zq, bar_q(buf),
+                                         once);
                     ++tau;
                 }
             }
@@ -580,6 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
+    } else if (warp >= 4 && *abort_flag) {
+        // This CTA gave up on a wait: every row of every unit it was given gets NaN in o and lse
+        // (all roles have stopped), so that none of them keeps a value that looks valid.  Each
+        // softmax warpgroup covers the rows of its own tile slot.
+        const int x = (warp - 4) >> 2;
+        const int r = threadIdx.x - 128 * (1 + x);
+        Unit u;
+        for (int round = 0; unit_at<CAUSAL>(p, round, u); ++round)
+            if (x == 0 || u.hasB) poison_row<D>(p, u.zq, (x ? u.tB : u.tA) * kBM + r);
     }
 }
 

@@ -317,7 +317,9 @@ def test_attention_convenience_matches(fa):
 @pytest.mark.parametrize("D", [64, 256])   # the two-tile kernel (D 64) and the one-tile kernel (D 256)
 def test_watchdog_reports_and_recovers(fa, orc, D):
     """An injected missing V load makes the bounded waits expire: the call reports
-    FA_ERR_DEVICE_TIMEOUT through fa_device_status and the context stays usable."""
+    FA_ERR_DEVICE_TIMEOUT through fa_device_status, every CTA that gave up leaves NaN in o and
+    lse of all the rows it was given (here every CTA skips its first V tile, so every row), and
+    the context stays usable."""
     w = Workload("wd", 1, 2, 2, 256, 256, D, "bf16", False, 5)
     q, k, v = (t.cuda() for t in make_qkv(w))
     o = torch.zeros_like(q)
@@ -326,6 +328,8 @@ def test_watchdog_reports_and_recovers(fa, orc, D):
     st, word = fa.fa_device_status()
     assert st == 12 and (word & 1) == 1, (st, word)
     assert ((word >> 8) & 0xFF) != 0
+    assert torch.isnan(lse).all().item(), "rows of an abandoned call must read NaN in lse"
+    assert torch.isnan(o).all().item(), "rows of an abandoned call must read NaN in o"
     # afterwards: a normal call is correct and the status word is clean
     o2, l2 = run_gpu(fa, w, q.cpu(), k.cpu(), v.cpu())
     o_ref, l_ref = orc.full(q.cpu(), k.cpu(), v.cpu(), False, False, w.softmax_scale)
