@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "schedule.h"
 
 namespace {
 
@@ -168,6 +169,7 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     p.inject = inject;
     p.o_al32 = aligned(o, 32) ? 1u : 0u;   // rows are 2*D bytes, so every row then starts on 32 bytes
     p.tau = tau;
+    fa::set_schedule_divisors(p);
 
     cudaError_t e = kernel >= 2 ? fa::launch_fwd1(D, key_tile, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream))
                                 : fa::launch_fwd(D, bf16, causal != 0, maps, p, reinterpret_cast<cudaStream_t>(stream));

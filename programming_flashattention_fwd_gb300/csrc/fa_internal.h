@@ -17,6 +17,13 @@ constexpr int kBN = 128;
 // instead of 8 saved 4 % of the time, and made no difference on unit-variance inputs.
 constexpr float kTauDefault = 12.0f;
 
+// Division by a divisor fixed for the launch, as a multiply-high and a shift (numerators below
+// 2^31): d, the multiplier m = floor(2^32 (2^l - d) / d) + 1 and the shift l = ceil(log2 d);
+// n / d == (umulhi(n, m) + n) >> l.  Filled on the host (make_fastdiv in schedule.h).
+struct FastDiv {
+    uint32_t d, mul, shr;
+};
+
 // Per-launch scalar parameters (passed by value to the kernel).
 struct Params {
     void *o;            // [B, Hq, Sq, D] 16-bit
@@ -33,6 +40,8 @@ struct Params {
     uint32_t inject;    // fault-injection mask (0 in normal use)
     uint32_t o_al32;    // o is 32-byte aligned: output rows are written in full 32-byte sectors
     float tau;          // lazy-rescale threshold (kTauDefault outside tests)
+    // the schedule's divisors (set_schedule_divisors in schedule.h): B*Hq, NP, Tq, Hq, Hq/Hkv
+    FastDiv f_nbh, f_np, f_tq, f_hq, f_group;
 };
 
 // The TMA descriptors: q, k, v as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.

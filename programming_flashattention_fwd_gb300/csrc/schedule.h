@@ -13,6 +13,36 @@
 
 namespace fa {
 
+// The multiplier and shift of FastDiv for divisor d >= 1 (host side).
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while (l < 31 && (1u << l) < d) ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return FastDiv{d, (uint32_t)m, l};
+}
+
+// n / d for 0 <= n < 2^31 (the sum below then stays under 2^32).
+__host__ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f)
+{
+#ifdef __CUDA_ARCH__
+    const uint32_t hi = __umulhi(n, f.mul);
+#else
+    const uint32_t hi = (uint32_t)(((uint64_t)n * f.mul) >> 32);
+#endif
+    return (hi + n) >> f.shr;
+}
+
+// Fills the schedule's divisors from B, Hq, group, Tq and NP (host side, before a launch).
+inline void set_schedule_divisors(Params &p)
+{
+    p.f_nbh = make_fastdiv((uint32_t)(p.B * p.Hq));
+    p.f_np = make_fastdiv((uint32_t)p.NP);
+    p.f_tq = make_fastdiv((uint32_t)p.Tq);
+    p.f_hq = make_fastdiv((uint32_t)p.Hq);
+    p.f_group = make_fastdiv((uint32_t)p.group);
+}
+
 // Index of the work unit that CTA c takes in round `round` (past the last unit when the
 // CTA has no more work).
 __host__ __device__ __forceinline__ long long unit_index(int G, int c, int round)
@@ -44,20 +74,22 @@ struct PairUnit {
 template <bool CAUSAL>
 __host__ __device__ __forceinline__ bool pair_unit(const Params &p, int G, int c, int round, PairUnit &u)
 {
-    const long long g = unit_index(G, c, round);
-    if (g >= p.num_units) return false;
+    const long long g64 = unit_index(G, c, round);
+    if (g64 >= p.num_units) return false;
+    const uint32_t g = (uint32_t)g64;   // below num_units < 2^31
     int bh, pr;
     if (CAUSAL) {   // heaviest query-tile pairs first
-        const int nbh = p.B * p.Hq;
-        pr = p.NP - 1 - (int)(g / nbh);
-        bh = (int)(g % nbh);
+        const uint32_t q = fdiv(g, p.f_nbh);
+        pr = p.NP - 1 - (int)q;
+        bh = (int)(g - q * p.f_nbh.d);
     } else {        // consecutive units share a head (and its K/V in L2)
-        bh = (int)(g / p.NP);
-        pr = (int)(g % p.NP);
+        const uint32_t q = fdiv(g, p.f_np);
+        bh = (int)q;
+        pr = (int)(g - q * p.f_np.d);
     }
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    u.zq = b * p.Hq + hq;
-    u.zkv = b * p.Hkv + hq / p.group;
+    const int b = (int)fdiv((uint32_t)bh, p.f_hq), hq = bh - b * p.Hq;
+    u.zq = bh;
+    u.zkv = b * p.Hkv + (int)fdiv((uint32_t)hq, p.f_group);
     u.tA = 2 * pr;
     u.tB = 2 * pr + 1;
     u.hasB = u.tB < p.Tq;
@@ -76,20 +108,22 @@ struct TileUnit {
 template <bool CAUSAL, int BN>
 __host__ __device__ __forceinline__ bool tile_unit(const Params &p, int G, int c, int round, TileUnit &u)
 {
-    const long long g = unit_index(G, c, round);
-    if (g >= p.num_units) return false;
+    const long long g64 = unit_index(G, c, round);
+    if (g64 >= p.num_units) return false;
+    const uint32_t g = (uint32_t)g64;   // below num_units < 2^31
     int bh, t;
     if (CAUSAL) {   // heaviest query tiles first
-        const int nbh = p.B * p.Hq;
-        t = p.Tq - 1 - (int)(g / nbh);
-        bh = (int)(g % nbh);
+        const uint32_t q = fdiv(g, p.f_nbh);
+        t = p.Tq - 1 - (int)q;
+        bh = (int)(g - q * p.f_nbh.d);
     } else {
-        bh = (int)(g / p.Tq);
-        t = (int)(g % p.Tq);
+        const uint32_t q = fdiv(g, p.f_tq);
+        bh = (int)q;
+        t = (int)(g - q * p.f_tq.d);
     }
-    const int b = bh / p.Hq, hq = bh % p.Hq;
-    u.zq = b * p.Hq + hq;
-    u.zkv = b * p.Hkv + hq / p.group;
+    const int b = (int)fdiv((uint32_t)bh, p.f_hq), hq = bh - b * p.Hq;
+    u.zq = bh;
+    u.zkv = b * p.Hkv + (int)fdiv((uint32_t)hq, p.f_group);
     u.t = t;
     u.nk = key_tiles(p, CAUSAL, t, BN);
     return true;

@@ -7,6 +7,7 @@
 // cover every key any of its rows may attend to and at most one key tile more (only a ragged
 // last query tile can over-reach, by its padding rows), and that every TMA coordinate the
 // kernels derive from a unit lies inside the tensors.  Prints "ok" or the first failure.
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <vector>
@@ -48,6 +49,7 @@ Params make_params(int B, int Hq, int Hkv, int Sq, int Sk, int causal, int key_t
     p.group = Hq / Hkv;
     p.num_units = pairs ? B * Hq * p.NP : B * Hq * p.Tq;
     p.coff = causal == 2 ? Sk - Sq : 0;
+    fa::set_schedule_divisors(p);
     return p;
 }
 
@@ -111,10 +113,45 @@ void check_shape(int B, int Hq, int Hkv, int Sq, int Sk, int causal, int G)
     }
 }
 
+// The launch's divisors (B*Hq, NP, Tq, Hq, Hq/Hkv) are applied as a multiply-high and a shift;
+// check that against exact division: every divisor up to 4096 on a spread of numerators, and
+// powers of two, their neighbours and large divisors near the 2^31 edge.
+void check_fastdiv()
+{
+    std::vector<uint32_t> divs;
+    for (uint32_t d = 1; d <= 4096; ++d) divs.push_back(d);
+    for (int k = 12; k <= 30; ++k)
+        for (int64_t e : {-1, 0, 1}) divs.push_back((uint32_t)((1ll << k) + e));
+    for (uint32_t d : {100000u, 999983u, 65537u, 1u << 30, 0x7fffffffu}) divs.push_back(d);
+    uint64_t x = 88172645463325252ull;   // xorshift64 for the random numerators
+    for (uint32_t d : divs) {
+        const fa::FastDiv f = fa::make_fastdiv(d);
+        auto check = [&](uint32_t n) {
+            if (n > 0x7fffffffu) return;
+            if (fa::fdiv(n, f) != n / d && fails++ < 20) std::printf("FAIL fastdiv: %u / %u\n", n, d);
+        };
+        for (uint32_t n = 0; n < 2048; ++n) check(n);
+        for (uint32_t k = 1; k < 64; ++k) {
+            const uint64_t m = (uint64_t)d * k;
+            if (m <= 0x80000000ull) { check((uint32_t)(m - 1)); check((uint32_t)m); check((uint32_t)(m + 1)); }
+        }
+        for (uint64_t k : {0x7fffffffull / d, 0x7fffffffull / d - 1}) {
+            const uint64_t m = k * d;
+            check((uint32_t)m); check((uint32_t)(m - 1 < m ? m - 1 : 0)); check((uint32_t)(m + d - 1));
+        }
+        check(0x7fffffffu);
+        for (int i = 0; i < 256; ++i) {
+            x ^= x << 13; x ^= x >> 7; x ^= x << 17;
+            check((uint32_t)(x & 0x7fffffffu));
+        }
+    }
+}
+
 } // namespace
 
 int main()
 {
+    check_fastdiv();
     const int seqs[] = {1, 17, 127, 128, 129, 255, 256, 257, 300, 513, 1000, 2000, 4096};
     const int heads[][2] = {{1, 1}, {2, 1}, {4, 2}, {8, 8}, {32, 8}, {6, 3}};
     const int grids[] = {1, 3, 152, 1000};
