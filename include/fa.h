@@ -127,8 +127,9 @@ int fa_device_status(fa_stream_t stream, uint32_t *detail);
 /*
  * fa_fwd_debug -- test hook: fa_fwd / fa_fwd_fp16 (is_fp16 selects) with an explicit
  * watchdog limit per wait (timeout_ns, 0 = the default of 2 s), a fault-injection mask
- * (inject bit 0: the load warp skips the first V tile, so the MMA warp's wait for it
- * expires; the kernel then records FA_ERR_DEVICE_TIMEOUT and every CTA returns normally),
+ * (inject bit 0: the load warp of every CTA skips its first V tile, so the MMA warp's wait for
+ * it expires; bit 1: only CTA 0 does; the kernel then records FA_ERR_DEVICE_TIMEOUT, the CTAs
+ * that gave up leave NaN in their rows of o and lse and every CTA returns normally),
  * the kernel variant (as fa_fwd_select) and the lazy-rescale threshold tau in log2 units
  * (O and l are rescaled only when the running row maximum grows by more than tau; 0 rescales
  * at every new maximum; negative = the default 12; above 15 -- where an unnormalised P could

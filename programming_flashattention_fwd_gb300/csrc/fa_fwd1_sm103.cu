@@ -155,14 +155,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ K/V producer (consumption order)
         if (lane == 0) {
             int use = 0;
-            int skip = -1;   // fault injection (inject bit 0): the first V tile is never loaded
+            int skip = -1;   // fault injection: the first V tile is never loaded (bit 0: every CTA; bit 1: CTA 0)
+            const bool inj = (p.inject & 1u) || ((p.inject & 2u) && blockIdx.x == 0);
             const uint64_t keep = l2_policy_evict_last();   // K/V tiles are read again by other tiles
             bool ok = true;
             auto load = [&](const CUtensorMap *m, int j, int zkv) {
                 const int s = use % C::NS;
                 if (!bounded_wait(bar_empty(s), ((use / C::NS) & 1) ^ 1, abort_flag, tmo, S_EMPTY, status))
                     return false;
-                if ((p.inject & 1u) && m == &tmV && skip < 0) {
+                if (inj && m == &tmV && skip < 0) {
                     skip = use++;
                     return true;
                 }

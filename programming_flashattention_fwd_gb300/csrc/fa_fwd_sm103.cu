@@ -62,7 +62,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 enum WaitSite : uint32_t {
     SITE_PROD_EMPTY = 1, SITE_MMA_Q = 2, SITE_MMA_FULL = 3, SITE_MMA_P = 4,
-    SITE_SM_S = 5, SITE_SM_O = 6, SITE_DRAIN = 7, SITE_QFREE = 8
+    SITE_SM_S = 5, SITE_SM_O = 6, SITE_DRAIN = 7, SITE_QFREE = 8, SITE_STAGED = 9
 };
 
 template <int D>
@@ -75,7 +75,7 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * TILE;
     static constexpr int OFF_BAR = OFF_RING + NS * TILE;
-    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 4 + 2 + 1;
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 4 + 2 + 1 + 1;   // ..., O[2], done, tile b staged
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
@@ -134,9 +134,14 @@ __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const Params p)
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p)
 {
     using C = Cfg<D>;
+    // Without the mask both tiles of a unit end on the same key step and their epilogues' row
+    // stores compete: tile b's rows then go out as bulk tensor stores staged in its finished
+    // query buffer (+2 % on the fp16 non-causal workload).  With the mask tile a ends a step
+    // earlier and that staging measured 0.4 % slower, so there both tiles store rows directly.
+    constexpr bool kStageB = !CAUSAL;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -157,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t barP0 = barS0 + 16u;                            // P_x keys [64h, 64h+64) written: + 16x + 8h
     const uint32_t barO0 = barS0 + 48u;                            // O_x final for the unit
     const uint32_t barDone = barS0 + 64u;
+    const uint32_t barStaged = barS0 + 72u;   // tile b's output rows staged in shared memory (4 warps)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -175,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(barO0, 1);
         mbar_init(barO0 + 8, 1);
         mbar_init(barDone, 1);
+        mbar_init(barStaged, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -186,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -197,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsLoad>();
         if (warp == 0 && lane == 0) {
             // ======================================================== K/V producer
-            const int skip = (p.inject & 1u) ? 1 : -1;   // ring use 1 = the first V tile
+            // fault injection: bit 0 -- every CTA skips its first V tile (ring use 1); bit 1 -- only CTA 0 does
+            const bool inj = (p.inject & 1u) || ((p.inject & 2u) && blockIdx.x == 0);
+            const int skip = inj ? 1 : -1;
             const uint64_t keep = l2_policy_evict_last(); // K/V tiles are read again by other tiles
             int use = 0;                                  // ring uses armed so far
             bool ok = true;
@@ -317,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_s(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE);
                     tc_commit_elect(barS0 + 8u * x);
-                    if (nk[x] == 1) tc_commit_elect(bar_qfree(buf[x]));
+                    // without the mask tile b's buffer is released by its softmax warps once the
+                    // output rows staged in it have been stored (its last S has completed by then)
+                    if (nk[x] == 1 && (x == 0 || !kStageB)) tc_commit_elect(bar_qfree(buf[x]));
                 }
                 if (!ok) break;
                 tc_commit_elect(bar_empty(uK0 % C::NS));
@@ -363,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             issue_s(tS[x], sQ + buf[x] * C::TILE, sKn);
                             tc_commit_elect(barS0 + 8u * x);
-                            if (j + 2 == nk[x]) tc_commit_elect(bar_qfree(buf[x]));
+                            if (j + 2 == nk[x] && (x == 0 || !kStageB)) tc_commit_elect(bar_qfree(buf[x]));
                         }
                     }
                     if (!ok) break;
@@ -388,9 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.sl2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t ks = 0, uo = 0;
+        int qt = 0;   // query tiles loaded so far (the Q producer's count: buffer of tile b = its index % NQ)
+        uint32_t ub = 0;   // tile b epilogues staged (barStaged phase)
         bool ok = true;
         Unit u;
         for (int round = 0; ok && unit_at<CAUSAL>(p, round, u); ++round) {
+            const int qb = qt + (u.nA > 0 ? 1 : 0);   // tile b's query-tile index (if it has keys)
+            qt = qb + (u.nB > 0 ? 1 : 0);
             if (x == 1 && !u.hasB) continue;
             const int t = x ? u.tB : u.tA;
             const int nk = x ? u.nB : u.nA;
@@ -570,7 +586,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   lo, hi);
                         pk[e] = pack2<BF16>(lo, hi);
                     }
-                    if (row < p.Sq) {
+                    if (kStageB && x == 1) {
+                        // tile b: rows staged in its finished query buffer (128B-swizzled, as the
+                        // tensor map expects), written out below by bulk tensor stores
+                        const uint32_t line = sQ + (uint32_t)(qb % C::NQ) * C::TILE + (uint32_t)(c / 64) * C::PANEL +
+                                              (uint32_t)r * 128u;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t chunk = (uint32_t)(((c & 63) >> 3) + i) ^ (uint32_t)(r & 7);
+                            st_shared_v4(line + (chunk << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
+                    } else if (row < p.Sq) {
                         if (p.o_al32) {   // full 32-byte sectors: half the store instructions, no partial sectors
                             st_global_v8(orow + c * 2, pk);
                             st_global_v8(orow + c * 2 + 32, pk + 8);
@@ -587,7 +613,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float lse = l > 0.f ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
                 p.lse[(size_t)u.zq * p.Sq + row] = lse;
             }
+            if (kStageB && x == 1) {
+                // Tile b's rows leave the SM as bulk tensor stores (rows >= Sq are clipped by the
+                // map), so the softmax warps do not wait for 2*D-byte row stores at the unit
+                // boundary, where tile b's epilogue is on the critical path.  Its query buffer is
+                // released to the Q producer once the stores have read it.
+                // every writer makes its rows visible to the copy engine, then each warp arrives;
+                // the storing thread's wait is bounded like every other (a warp that gave up on an
+                // earlier wait never arrives, and then no store is issued)
+                fence_proxy_async_smem();
+                __syncwarp();
+                mbar_arrive_elect(barStaged);
+                if (r == 0 && wait_bar(barStaged, ub & 1, abort_flag, tmo, SITE_STAGED)) {
+                    const uint32_t sb_b = sQ + (uint32_t)(qb % C::NQ) * C::TILE;
+#pragma unroll
+                    for (int pn = 0; pn < C::PANELS; ++pn) tma_store_3d(&tmO, pn * 64, t * kBM, u.zq, sb_b + pn * C::PANEL);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                    mbar_arrive(bar_qfree(qb % C::NQ));
+                }
+                ++ub;
+            }
         }
+        if (kStageB && x == 1 && r == 0) tma_store_wait_all();   // every output store has landed before the CTA exits
     }
 
     tc_fence_before();
@@ -640,7 +688,7 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
     Params q = p;
     if (q.timeout_ns == 0) q.timeout_ns = kDefaultTimeoutNs;
     const int grid = min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
-    kern<<<grid, kThreads, smem, stream>>>(m.q, m.k, m.v, q);
+    kern<<<grid, kThreads, smem, stream>>>(m.q, m.k, m.v, m.o, q);
     return cudaGetLastError();
 }
 

@@ -44,9 +44,10 @@ struct Params {
     FastDiv f_nbh, f_np, f_tq, f_hq, f_group;
 };
 
-// The TMA descriptors: q, k, v as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle.
+// The TMA descriptors: q, k, v, o as 3-D (D, S, B*H) tensors, 64 x 128 boxes, 128B swizzle
+// (o: the two-tile kernel writes tile b's output rows with bulk tensor stores).
 struct Maps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
 };
 
 // Checks shared by the entry points, made before any CUDA call: the argument checks of

@@ -17,7 +17,8 @@ same (rounded) inputs.
     and non-default scales, input std), every row checked;
   - bitwise determinism and a non-default stream;
   - the watchdog: an injected missing load makes the kernel give up, report
-    FA_ERR_DEVICE_TIMEOUT and return; the context stays usable.
+    FA_ERR_DEVICE_TIMEOUT and return, with NaN in o and lse of exactly the rows of the CTAs
+    that gave up; the context stays usable.
 """
 import math
 import zlib
@@ -334,6 +335,32 @@ def test_watchdog_reports_and_recovers(fa, orc, D):
     o2, l2 = run_gpu(fa, w, q.cpu(), k.cpu(), v.cpu())
     o_ref, l_ref = orc.full(q.cpu(), k.cpu(), v.cpu(), False, False, w.softmax_scale)
     check(o2, l2, o_ref, l_ref, "after watchdog")
+    assert fa.fa_device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("D", [64, 256])
+def test_watchdog_nan_marks_only_the_abandoned_rows(fa, orc, D):
+    """inject bit 1: only CTA 0 skips its first V tile.  That CTA gives up; its rows read NaN in o
+    and lse, and every other row -- computed by CTAs that finished -- matches the oracle.  With
+    B=1, Hq=Hkv=4, S=512 and no mask CTA 0 takes one unit: query tiles 0 and 1 of head 0 for the
+    two-tile kernel (D = 64, 8 units on 8 CTAs), query tile 0 of head 0 for the one-tile kernel
+    (D = 256, 16 units on 16 CTAs)."""
+    w = Workload("wd1", 1, 4, 4, 512, 512, D, "bf16", False, 6)
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.zeros_like(qd)
+    lse = torch.zeros(qd.shape[:3], dtype=torch.float32, device="cuda")
+    fa.fa_fwd_debug(qd, kd, vd, o, lse, False, w.softmax_scale, timeout_ns=20_000_000, inject=2)
+    st, word = fa.fa_device_status()
+    assert st == 12 and (word & 1) == 1, (st, word)
+    oc, lc = o.cpu(), lse.cpu()
+    bad = torch.zeros(lc.shape, dtype=torch.bool)
+    bad[0, 0, :(256 if D <= 128 else 128)] = True
+    assert torch.isnan(lc[bad]).all().item() and torch.isnan(oc[bad]).all().item()
+    assert torch.isfinite(lc[~bad]).all().item() and torch.isfinite(oc[~bad]).all().item()
+    o_ref, l_ref = orc.full(q, k, v, False, False, w.softmax_scale)
+    keep = (~bad).numpy()
+    check(oc[~bad], lc[~bad], o_ref[keep], l_ref[keep], "rows of the CTAs that finished")
     assert fa.fa_device_status() == (0, 0)
 
 
