@@ -548,7 +548,7 @@ def run_ours(args, workloads, world, rank, local):
                  "roofline": roofline_record(w, args, rec["t_step"]), "clocks": rec["clocks"],
                  "timing": timing_record(rec, w, world), "gpu_launches": args.steps,
                  "target_frac": TARGET_FRAC if w.D == 128 else None}
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:   # the oracle baseline is timed at N = 1 only
             budget = args.cpu_seconds if i == 0 else args.cpu_seconds_per_config
             entry["cpu_baseline"] = time_oracle(w, *host, budget, seed=w.seed + 100)
         per_config[w.name] = entry
