@@ -33,7 +33,9 @@
 // range; O and l always share the same stale max, so the result is unchanged); a negative
 // scale negates S inside the MMA and a zero scale zeroes Q at load time; K/V tails and the causal diagonal are masked only
 // on the tiles that need it; fully masked causal tiles are skipped; the log-sum-exp is
-// written out; output rows go out in full 32-byte sectors when o is 32-byte aligned.
+// written out; output rows go out in full 32-byte sectors when o is 32-byte aligned, except
+// that without the mask tile b's rows are staged in its finished query buffer and written by
+// bulk tensor stores; K/V loads carry an L2 evict_last hint and query loads evict_first.
 //
 // Every wait is bounded (watchdog): on expiry the kernel records a status word, raises a
 // CTA-wide abort flag, lets its own copies and MMAs drain, frees TMEM, writes NaN into o and lse
@@ -615,12 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (kStageB && x == 1) {
                 // Tile b's rows leave the SM as bulk tensor stores (rows >= Sq are clipped by the
-                // map), so the softmax warps do not wait for 2*D-byte row stores at the unit
-                // boundary, where tile b's epilogue is on the critical path.  Its query buffer is
-                // released to the Q producer once the stores have read it.
-                // every writer makes its rows visible to the copy engine, then each warp arrives;
-                // the storing thread's wait is bounded like every other (a warp that gave up on an
-                // earlier wait never arrives, and then no store is issued)
+                // map), so its softmax warps do not stall on 2*D-byte row stores while tile a's
+                // epilogue stores its own rows.  Every writer makes its rows visible to the copy
+                // engine and each warp arrives; the storing thread's wait is bounded like every
+                // other (a warp that gave up on an earlier wait never arrives, and then no store
+                // is issued).  The query buffer goes back to the Q producer once the stores have
+                // read it; it holds the query tile of the unit after next.
                 fence_proxy_async_smem();
                 __syncwarp();
                 mbar_arrive_elect(barStaged);
