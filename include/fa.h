@@ -90,9 +90,10 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * measured per workload).  Same results up to rounding order.
  *   kernel 0: automatic -- 1 for D <= 128, 2 for D = 256 (what fa_fwd does)
  *   kernel 1: two 128-row query tiles per CTA sharing 128-key steps (D 64 or 128)
- *   kernel 2: one 128-row query tile per CTA, 64-key steps, double-buffered scores (D 128 or 256;
- *             the block-size trade of the guide's troubleshooting item, and the only layout
- *             that fits D = 256 in tensor memory)
+ *   kernel 2: one 128-row query tile per CTA, 64-key steps, double-buffered scores (D 64, 128 or
+ *             256; the block-size trade of the guide's troubleshooting item, and the only
+ *             layout that fits D = 256 in tensor memory; at D = 64 two CTAs share an SM and
+ *             every query tile gets its own CTA, heaviest first)
  *   kernel 3: one 128-row query tile per CTA, 128-key steps, double-buffered scores (D 128)
  * An unsupported (kernel, D) pair returns FA_ERR_UNSUPPORTED_D; kernel or dtype out of range
  * returns FA_ERR_ARG.

@@ -88,7 +88,7 @@ int check_fwd_args(const void *q, const void *k, const void *v, const void *o, c
     if (kernel < 0 || kernel > 3) return FA_ERR_ARG;
     if (kernel == 0) kernel = (D == 256) ? 2 : 1;
     if (kernel == 1 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
-    if (kernel == 2 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED_D;
+    if (kernel == 2 && D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED_D;
     if (kernel == 3 && D != 128) return FA_ERR_UNSUPPORTED_D;
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
     if (causal < 0 || causal > 2) return FA_ERR_CAUSAL;
@@ -113,7 +113,7 @@ int check_fwd_args(const void *q, const void *k, const void *v, const void *o, c
 namespace {
 
 // kernel: 0 = automatic (two-tile for D <= 128, one-tile for D = 256), 1 = two query tiles per
-// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 128 / 256),
+// CTA with 128-key steps (D 64 / 128), 2 = one query tile per CTA with 64-key steps (D 64 / 128 / 256),
 // 3 = one query tile per CTA with 128-key steps (D 128); kernels 2 and 3 double-buffer the scores.
 int run(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk,
         int D, int causal, float scale, fa_stream_t stream, bool bf16, uint64_t timeout_ns, uint32_t inject,

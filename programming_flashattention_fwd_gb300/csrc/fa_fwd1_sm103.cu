@@ -70,7 +70,11 @@ struct Cfg {
     static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 1 + 1 + 1;   // q, qfree, full, empty, S[2], P, PV, done
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
-    static constexpr int ALLOC = (BYTES + 1024 <= 232448) ? BYTES + 1024 : 232448;
+    // at D = 64 at least 80 KB, so that no third CTA is co-resident on an SM (two allocations of
+    // 256 tensor-memory columns fill it)
+    static constexpr int ALLOC_MIN = (D == 64) ? 80 * 1024 : 0;
+    static constexpr int ALLOC_RAW = (BYTES + 1024 <= 232448) ? BYTES + 1024 : 232448;
+    static constexpr int ALLOC = ALLOC_RAW > ALLOC_MIN ? ALLOC_RAW : ALLOC_MIN;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN;
     static constexpr uint32_t TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
 };
@@ -95,8 +99,13 @@ __device__ __forceinline__ bool unit_at(const Params &p, int round, Unit &u)
     return tile_unit<CAUSAL, BN>(p, gridDim.x, blockIdx.x, round, u);
 }
 
+// At D = 64 a CTA needs 192 tensor-memory columns (a 256-column allocation) and ~74 KB of shared
+// memory, so two CTAs share an SM; the launch then gives every query tile its own CTA.
+template <int D>
+constexpr int kMinBlocks = (D == 64) ? 2 : 1;
+
 template <int D, int KEYS, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
     fa_fwd1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p)
 {
@@ -486,7 +495,9 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
     }
     Params q = p;
     if (q.timeout_ns == 0) q.timeout_ns = kDefaultTimeoutNs;
-    const int grid = min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
+    // D = 64: one CTA per query tile (two resident per SM), issued heaviest first, so the block
+    // scheduler balances the causal tiles of unequal length; otherwise one persistent CTA per SM.
+    const int grid = (D == 64) ? p.num_units : min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
     kern<<<grid, THREADS, Cfg<D, KEYS>::ALLOC, stream>>>(m.q, m.k, m.v, q);
     return cudaGetLastError();
 }
@@ -497,6 +508,7 @@ cudaError_t launch_fwd1(int D, int keys, bool bf16, bool causal, const Maps &m, 
 {
 #define F1_CASE(DD, KK, BB, CC) \
     if (D == DD && keys == KK && bf16 == BB && causal == CC) return one::launch_one<DD, KK, BB, CC>(m, p, st);
+    F1_CASE(64, 64, true, false) F1_CASE(64, 64, true, true) F1_CASE(64, 64, false, false) F1_CASE(64, 64, false, true)
     F1_CASE(128, 64, true, false) F1_CASE(128, 64, true, true) F1_CASE(128, 64, false, false) F1_CASE(128, 64, false, true)
     F1_CASE(128, 128, true, false) F1_CASE(128, 128, true, true) F1_CASE(128, 128, false, false) F1_CASE(128, 128, false, true)
     F1_CASE(256, 64, true, false) F1_CASE(256, 64, true, true) F1_CASE(256, 64, false, false) F1_CASE(256, 64, false, true)

@@ -63,10 +63,10 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const Maps &maps, const Pa
 // Reads and clears the current device's watchdog word (synchronous on `stream`).
 cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *word);
 
-// One query tile per CTA, 64-key steps, double-buffered scores (D = 128 or 256).  K/V maps
+// One query tile per CTA, 64-key steps, double-buffered scores (D = 64, 128 or 256).  K/V maps
 // use 64-row boxes; Params.Tk counts 64-key tiles and num_units = B * Hq * Tq.
 cudaError_t launch_fwd1(int D, int keys, bool bf16, bool causal, const Maps &maps, const Params &p,
-                        cudaStream_t stream);   // keys per step: 64 (D 128 / 256) or 128 (D 128)
+                        cudaStream_t stream);   // keys per step: 64 (D 64 / 128 / 256) or 128 (D 128)
 cudaError_t read_and_clear_fa1_status(uint32_t *word);
 
 // ---------------------------------------------------------------- tiled matrix product

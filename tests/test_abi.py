@@ -161,7 +161,7 @@ def test_softmax_invalid_arguments(lib, args, code):
 
 @pytest.mark.parametrize("D,dtype,kernel,code", [
     (128, 0, 4, 15), (128, 2, 1, 15), (128, 0, -1, 15),
-    (256, 0, 1, 4), (64, 1, 2, 4), (192, 0, 0, 4), (256, 0, 3, 4), (64, 0, 3, 4),
+    (256, 0, 1, 4), (192, 0, 0, 4), (256, 0, 3, 4), (64, 0, 3, 4), (192, 1, 2, 4),
 ])
 def test_select_invalid_arguments(lib, D, dtype, kernel, code):
     assert lib.fa_fwd_select(Q, K, V, O, L, 1, 4, 2, 256, 256, D, 1, 0.1, None, dtype, kernel) == code
@@ -170,7 +170,7 @@ def test_select_invalid_arguments(lib, D, dtype, kernel, code):
 def test_select_valid_pairs_pass_validation(lib):
     # every supported (kernel, D) pair gets past validation: an overlapping lse makes each
     # call stop at the overlap check instead, before any CUDA call
-    for kernel, D in ((0, 64), (0, 128), (0, 256), (1, 64), (1, 128), (2, 128), (2, 256), (3, 128)):
+    for kernel, D in ((0, 64), (0, 128), (0, 256), (1, 64), (1, 128), (2, 64), (2, 128), (2, 256), (3, 128)):
         assert lib.fa_fwd_select(Q, K, V, O, O + 16, 1, 4, 2, 256, 256, D, 1, 0.1, None, 0, kernel) == 6
 
 

@@ -115,7 +115,7 @@ def test_shape_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal):
 
 
 SWEEP_ONE = []
-for D, kernel in ((128, 2), (256, 0), (128, 3)):
+for D, kernel in ((128, 2), (256, 0), (128, 3), (64, 2)):
     for (B, Hq, Hkv, Sq, Sk) in [(1, 1, 1, 1, 1), (1, 2, 1, 63, 63), (1, 2, 2, 64, 65), (2, 4, 2, 129, 129),
                                  (1, 3, 3, 300, 300), (1, 4, 2, 384, 200), (1, 2, 1, 200, 384),
                                  (1, 2, 1, 513, 100), (1, 2, 2, 1, 300)]:
@@ -126,8 +126,9 @@ for D, kernel in ((128, 2), (256, 0), (128, 3)):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,kernel", SWEEP_ONE)
 def test_one_tile_kernel_sweep(fa, orc, dtype, B, Hq, Hkv, Sq, Sk, D, causal, kernel):
-    """The one-query-tile kernel: 64-key steps at D = 256 (the automatic choice) and at D = 128
-    (fa_fwd_select kernel 2), 128-key steps at D = 128 (kernel 3); every row checked."""
+    """The one-query-tile kernel: 64-key steps at D = 256 (the automatic choice) and at D = 128 or
+    64 (fa_fwd_select kernel 2; at D = 64 two CTAs share an SM, one per query tile), 128-key steps
+    at D = 128 (kernel 3); every row checked."""
     seed = zlib.crc32(repr(("one", B, Hq, Hkv, Sq, Sk, D, causal, dtype) + ((kernel,) if kernel == 3 else ())).encode()) % 100000
     w = Workload("sweep1", B, Hq, Hkv, Sq, Sk, D, dtype, causal, seed,
                  q_std=2.0 if dtype == "fp16" else 1.0, k_std=2.0 if dtype == "fp16" else 1.0)
