@@ -105,6 +105,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return false;
 }
 
+// One probe of a phase by the whole (converged) warp, combined by a warp vote: true when the
+// phase has completed for every lane.  The fast path of a warp-uniform wait, without a per-lane
+// branch before the vote.
+__device__ __forceinline__ bool mbar_try_wait_all(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "vote.sync.all.pred q, p, 0xffffffff;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
 // One arrival on `bar` by one elected lane of the (converged) warp, without a branch.
 __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar)
 {
@@ -122,6 +138,84 @@ __device__ __forceinline__ void poison_row(const Params &p, int zq, int row)
 #pragma unroll 1
     for (int c = 0; c < D * 2; c += 16) st_global_v4(orow + c, ~0u, ~0u, ~0u, ~0u);
     p.lse[(size_t)zq * p.Sq + row] = __uint_as_float(~0u);
+}
+
+// S = Q K^T at D = 128 in one block: both 64-column panels (eight 16-column K-steps; the second
+// panel's operands start PANEL_OFF 16-byte units further) behind a single elect.sync, followed
+// by the commit that tells the softmax warps S is ready -- fewer instructions for the MMA warp,
+// which shares its SM sub-partition with two softmax warps.
+template <uint32_t PANEL_OFF, bool TWO = false>
+__device__ __forceinline__ void mma_s_d128_commit_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                        uint32_t idesc, uint32_t bar, uint32_t bar2 = 0)
+{
+    if constexpr (TWO) {   // ... and a second commit (the K slot the MMAs read), same elected lane
+        asm volatile("{\n\t.reg .b32 al, bl;\n\t.reg .b64 a, b;\n\t.reg .pred e, f, t;\n\t"
+                     "setp.eq.b32 t, 0, 0;\n\tsetp.ne.b32 f, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                     "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, f;\n\t"
+                     "add.u32 al, %1, 2;\n\tadd.u32 bl, %2, 2;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "add.u32 al, %1, 4;\n\tadd.u32 bl, %2, 4;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "add.u32 al, %1, 6;\n\tadd.u32 bl, %2, 6;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "add.u32 al, %1, %7;\n\tadd.u32 bl, %2, %7;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "add.u32 al, %1, %8;\n\tadd.u32 bl, %2, %8;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "add.u32 al, %1, %9;\n\tadd.u32 bl, %2, %9;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "add.u32 al, %1, %10;\n\tadd.u32 bl, %2, %10;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                     "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+                     "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+                     ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(bar), "r"(bar2), "n"(PANEL_OFF),
+                       "n"(PANEL_OFF + 2), "n"(PANEL_OFF + 4), "n"(PANEL_OFF + 6)
+                     : "memory");
+        return;
+    }
+    asm volatile("{\n\t.reg .b32 al, bl;\n\t.reg .b64 a, b;\n\t.reg .pred e, f, t;\n\t"
+                 "setp.eq.b32 t, 0, 0;\n\tsetp.ne.b32 f, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, f;\n\t"
+                 "add.u32 al, %1, 2;\n\tadd.u32 bl, %2, 2;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "add.u32 al, %1, 4;\n\tadd.u32 bl, %2, 4;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "add.u32 al, %1, 6;\n\tadd.u32 bl, %2, 6;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "add.u32 al, %1, %6;\n\tadd.u32 bl, %2, %6;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "add.u32 al, %1, %7;\n\tadd.u32 bl, %2, %7;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "add.u32 al, %1, %8;\n\tadd.u32 bl, %2, %8;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "add.u32 al, %1, %9;\n\tadd.u32 bl, %2, %9;\n\tmov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
+                 ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(bar), "n"(PANEL_OFF), "n"(PANEL_OFF + 2),
+                   "n"(PANEL_OFF + 4), "n"(PANEL_OFF + 6)
+                 : "memory");
+}
+
+// O += P V for one 64-key half (four 16-key steps, as mma_ts_mn4_elect) followed by a commit to
+// `bar` from the same elected lane.
+__device__ __forceinline__ void mma_pv_commit_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                    uint32_t idesc, uint32_t accumulate, uint32_t bar)
+{
+    asm volatile("{\n\t.reg .b32 ta, bl;\n\t.reg .b64 b;\n\t.reg .pred p, e, t;\n\t"
+                 "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "mov.b64 b, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t"
+                 "add.u32 ta, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+                 "add.u32 ta, %1, 16;\n\tadd.u32 bl, %2, 256;\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+                 "add.u32 ta, %1, 24;\n\tadd.u32 bl, %2, 384;\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "r"(bar)
+                 : "memory");
 }
 
 // One work unit, decoded identically by every role (the schedule is in schedule.h).
@@ -273,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t HI = sdesc_hi_sw128(1024);   // 8-row groups 1024 bytes apart
             const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
             const uint32_t tO[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
-            auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) {
-                return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, tmo, site));
+            auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+                if (mbar_try_wait_all(bar, parity)) return true;   // the usual case: already complete
+                return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, tmo, site)) != 0;
             };
 
             // S = Q K^T: A = Q tile, B = K tile, both K-major (rows of D contiguous
@@ -287,6 +382,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss_kk4_elect(dS, qlo + off, klo + off, HI, idS, pn > 0);
                 }
             };
+            // the same followed by commits to `bar` and `bar2` (at D = 128 in one block, one elect.sync)
+            auto issue_s_commit2 = [&](uint32_t dS, uint32_t sQt, uint32_t sK, uint32_t bar, uint32_t bar2) {
+                if constexpr (D == 128) {
+                    constexpr uint32_t kPanelOff = (uint32_t)C::PANEL / 16;
+                    mma_s_d128_commit_elect<kPanelOff, true>(dS, sdesc_lo(sQt, 16), sdesc_lo(sK, 16), HI, idS, bar, bar2);
+                } else {
+                    issue_s(dS, sQt, sK);
+                    tc_commit_elect(bar);
+                    tc_commit_elect(bar2);
+                }
+            };
+            // the same followed by the commit to `bar` (at D = 128 in one block, one elect.sync)
+            auto issue_s_commit = [&](uint32_t dS, uint32_t sQt, uint32_t sK, uint32_t bar) {
+                if constexpr (D == 128) {
+                    constexpr uint32_t kPanelOff = (uint32_t)C::PANEL / 16;
+                    mma_s_d128_commit_elect<kPanelOff>(dS, sdesc_lo(sQt, 16), sdesc_lo(sK, 16), HI, idS, bar);
+                } else {
+                    issue_s(dS, sQt, sK);
+                    tc_commit_elect(bar);
+                }
+            };
             // O += P V for keys [64h, 64h+64): A = P from TMEM (16-bit pairs per column),
             // B = V tile, MN-major (D contiguous per key row): 8-key groups 1024 bytes apart,
             // 64-column panels C::PANEL bytes apart; 16 keys per K-step.
@@ -294,6 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t vlo = sdesc_lo(sV, C::PANEL);
                 mma_ts_mn4_elect(dO, tP + 32 * h, vlo + (uint32_t)((4 * h * 2048) >> 4), HI, idPV,
                                  (first && h == 0) ? 0u : 1u);
+            };
+            // tile b's second half releases the V slot in the same block (its P V are the last readers)
+            auto issue_pv_half_commit = [&](uint32_t dO, uint32_t tP, uint32_t sV, uint32_t bar) {
+                const uint32_t vlo = sdesc_lo(sV, C::PANEL);
+                mma_pv_commit_elect(dO, tP + 32, vlo + (uint32_t)((4 * 2048) >> 4), HI, idPV, 1u, bar);
             };
 
             int use = 0;               // ring uses consumed (K_j = use, V_j = use + 1 within a step)
@@ -327,8 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    issue_s(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE);
-                    tc_commit_elect(barS0 + 8u * x);
+                    issue_s_commit(tS[x], sQ + buf[x] * C::TILE, sRing + (uK0 % C::NS) * C::TILE, barS0 + 8u * x);
                     // without the mask tile b's buffer is released by its softmax warps once the
                     // output rows staged in it have been stored (its last S has completed by then)
                     if (nk[x] == 1 && (x == 0 || !kStageB)) tc_commit_elect(bar_qfree(buf[x]));
@@ -361,13 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ok = wait_u(barP0 + 16u * x + 8u * h, ks[x] & 1, SITE_MMA_P);
                                 if (!ok) break;
                                 tc_fence_after();
-                                issue_pv_half(tO[x], tS[x], sV, h, j == 0);
+                                if (x == nt - 1 && h == 1)
+                                    issue_pv_half_commit(tO[x], tS[x], sV, bar_empty(uV % C::NS));
+                                else
+                                    issue_pv_half(tO[x], tS[x], sV, h, j == 0);
                             }
                             if (!ok) break;
                             ++ks[x];
                             if (j == nk[x] - 1) tc_commit_elect(barO0 + 8u * x);
+                        } else if (x == nt - 1) {
+                            tc_commit_elect(bar_empty(uV % C::NS));   // tile b has no step j
                         }
-                        if (x == nt - 1) tc_commit_elect(bar_empty(uV % C::NS));
                         if (j + 1 < nk[x]) {
                             if (!kn_ready) {
                                 ok = wait_u(bar_full(uKn % C::NS), (uKn / C::NS) & 1, SITE_MMA_FULL);
@@ -375,13 +499,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc_fence_after();
                                 kn_ready = true;
                             }
-                            issue_s(tS[x], sQ + buf[x] * C::TILE, sKn);
-                            tc_commit_elect(barS0 + 8u * x);
+                            // tile b's S is the last reader of K_{j+1}: release its slot in the same block
+                            if (x == nt - 1)
+                                issue_s_commit2(tS[x], sQ + buf[x] * C::TILE, sKn, barS0 + 8u * x, bar_empty(uKn % C::NS));
+                            else
+                                issue_s_commit(tS[x], sQ + buf[x] * C::TILE, sKn, barS0 + 8u * x);
                             if (j + 2 == nk[x] && (x == 0 || !kStageB)) tc_commit_elect(bar_qfree(buf[x]));
                         }
                     }
                     if (!ok) break;
-                    if (more) tc_commit_elect(bar_empty(uKn % C::NS));
+                    if (more && !(j + 1 < nk[nt - 1])) tc_commit_elect(bar_empty(uKn % C::NS));   // tile b had no S(j+1)
                     use += 2;
                 }
             }
@@ -427,7 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY;  // running max in exp2 units (possibly stale by <= p.tau)
             float l = 0.f;             // running sum of p at m_used
             for (int j = 0; j < nk; ++j) {
-                ok = __all_sync(0xffffffffu, wait_bar(barS, ks & 1, abort_flag, tmo, SITE_SM_S));
+                ok = mbar_try_wait_all(barS, ks & 1) ||
+                     __all_sync(0xffffffffu, wait_bar(barS, ks & 1, abort_flag, tmo, SITE_SM_S)) != 0;
                 if (!ok) break;
                 ++ks;
                 tc_fence_after();
@@ -556,7 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---- epilogue: O / l -> 16-bit -> global (one 2*D-byte row per thread), and lse
-            ok = __all_sync(0xffffffffu, wait_bar(barO, uo & 1, abort_flag, tmo, SITE_SM_O));
+            ok = mbar_try_wait_all(barO, uo & 1) ||
+                 __all_sync(0xffffffffu, wait_bar(barO, uo & 1, abort_flag, tmo, SITE_SM_O)) != 0;
             if (!ok) break;
             ++uo;
             tc_fence_after();
