@@ -79,6 +79,79 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
 };
 
+// One probe of a phase by the whole (converged) warp, combined by a warp vote (the fast path of
+// a warp-uniform wait, without a per-lane branch before the vote).
+__device__ __forceinline__ bool mbar_try_wait_all(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "vote.sync.all.pred q, p, 0xffffffff;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// S = Q K^T over all NP 64-column panels of D (four 16-column K-steps each; the panels of Q and K
+// start QOFF and KOFF 16-byte units apart) behind one elect.sync, followed by two commits from the
+// same elected lane (S ready; the K slot released): fewer instructions for the MMA warp, which
+// shares its SM sub-partition with a softmax warp.
+#define F1_S_STEP(OFF) "add.u32 al, qa, " #OFF ";\n\tadd.u32 bl, ka, " #OFF ";\n\t"                        \
+                       "mov.b64 a, {al, %3};\n\tmov.b64 b, {bl, %3};\n\t"                                   \
+                       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, t;\n\t"
+#define F1_S_PANEL(ACC) "mov.b64 a, {qa, %3};\n\tmov.b64 b, {ka, %3};\n\t"                                  \
+                        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, " #ACC ";\n\t"                 \
+                        F1_S_STEP(2) F1_S_STEP(4) F1_S_STEP(6)
+#define F1_S_NEXT "add.u32 qa, qa, %7;\n\tadd.u32 ka, ka, %8;\n\t" F1_S_PANEL(t)
+#define F1_S_HEAD "{\n\t.reg .b32 qa, ka, al, bl;\n\t.reg .b64 a, b;\n\t.reg .pred e, f, t;\n\t"          \
+                  "setp.eq.b32 t, 0, 0;\n\tsetp.ne.b32 f, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"          \
+                  "mov.b32 qa, %1;\n\tmov.b32 ka, %2;\n\t" F1_S_PANEL(f)
+#define F1_S_TAIL "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"        \
+                  "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+template <int NP, uint32_t QOFF, uint32_t KOFF>
+__device__ __forceinline__ void mma_s_commit2_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                    uint32_t idesc, uint32_t bar1, uint32_t bar2)
+{
+    static_assert(NP == 1 || NP == 2 || NP == 4, "64-column panels of D");
+    if constexpr (NP == 1)
+        asm volatile(F1_S_HEAD F1_S_TAIL ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(bar1),
+                     "r"(bar2), "n"(QOFF), "n"(KOFF) : "memory");
+    else if constexpr (NP == 2)
+        asm volatile(F1_S_HEAD F1_S_NEXT F1_S_TAIL ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc),
+                     "r"(bar1), "r"(bar2), "n"(QOFF), "n"(KOFF) : "memory");
+    else
+        asm volatile(F1_S_HEAD F1_S_NEXT F1_S_NEXT F1_S_NEXT F1_S_TAIL ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi),
+                     "r"(idesc), "r"(bar1), "r"(bar2), "n"(QOFF), "n"(KOFF) : "memory");
+}
+#undef F1_S_STEP
+#undef F1_S_PANEL
+#undef F1_S_NEXT
+#undef F1_S_HEAD
+#undef F1_S_TAIL
+
+// O += P V over 64 keys (four 16-key steps, as mma_ts_mn4_elect) followed by two commits from
+// the same elected lane (P V done; the V slot released).
+__device__ __forceinline__ void mma_pv_commit2_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                     uint32_t idesc, uint32_t accumulate, uint32_t bar1, uint32_t bar2)
+{
+    asm volatile("{\n\t.reg .b32 ta, bl;\n\t.reg .b64 b;\n\t.reg .pred p, e, t;\n\t"
+                 "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "mov.b64 b, {%2, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t"
+                 "add.u32 ta, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+                 "add.u32 ta, %1, 16;\n\tadd.u32 bl, %2, 256;\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+                 "add.u32 ta, %1, 24;\n\tadd.u32 bl, %2, 384;\n\tmov.b64 b, {bl, %3};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "r"(bar1), "r"(bar2)
+                 : "memory");
+}
+
 // One work unit, decoded identically by every role (the schedule is in schedule.h).
 using Unit = TileUnit;
 
@@ -228,25 +301,28 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         const uint32_t idS = idesc_f16(BF16, BM, BN, false) | (p.smode == 1 ? kNegateA : 0u);
         constexpr uint32_t idPV = idesc_f16(BF16, BM, D, true);
         constexpr uint32_t HI = sdesc_hi_sw128(1024);
-        auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) {
-            return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_flag, tmo, site, status));
+        auto wait_u = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+            if (mbar_try_wait_all(bar, parity)) return true;   // the usual case: already complete
+            return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_flag, tmo, site, status)) != 0;
         };
-        // S = Q K^T over D (both K-major, 16 columns of D per instruction)
-        auto issue_s = [&](uint32_t dS, uint32_t sQt, uint32_t sK) {
-            const uint32_t qlo = sdesc_lo(sQt, 16), klo = sdesc_lo(sK, 16);
-#pragma unroll
-            for (int pn = 0; pn < D / 64; ++pn)   // 4 K-steps per 64-column panel
-                mma_ss_kk4_elect(dS, qlo + (uint32_t)((pn * C::QPANEL) >> 4), klo + (uint32_t)((pn * C::KVPANEL) >> 4),
-                                 HI, idS, pn > 0);
+        // S = Q K^T over D (both K-major, 16 columns of D per instruction), then the commits for
+        // S ready and the K slot released, all in one block
+        auto issue_s_commit2 = [&](uint32_t dS, uint32_t sQt, uint32_t sK, uint32_t bar1, uint32_t bar2) {
+            mma_s_commit2_elect<D / 64, (uint32_t)C::QPANEL / 16, (uint32_t)C::KVPANEL / 16>(
+                dS, sdesc_lo(sQt, 16), sdesc_lo(sK, 16), HI, idS, bar1, bar2);
         };
         // O += P V over BN keys: A = P from TMEM, B = V (MN-major, 64-column panels C::KVPANEL
-        // apart); one group of four 16-key steps per 64 keys
-        auto issue_pv = [&](uint32_t tP, uint32_t sV, bool first) {
+        // apart); one group of four 16-key steps per 64 keys, the last group followed by the
+        // commits for P V done and the V slot released
+        auto issue_pv_commit2 = [&](uint32_t tP, uint32_t sV, bool first, uint32_t bar1, uint32_t bar2) {
             const uint32_t vlo = sdesc_lo(sV, C::KVPANEL);
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h)
+            for (int h = 0; h + 1 < BN / 64; ++h)
                 mma_ts_mn4_elect(tmem + C::COL_O, tP + 32 * h, vlo + (uint32_t)((4 * h * 2048) >> 4), HI, idPV,
                                  (first && h == 0) ? 0u : 1u);
+            constexpr int hl = BN / 64 - 1;
+            mma_pv_commit2_elect(tmem + C::COL_O, tP + 32 * hl, vlo + (uint32_t)((4 * hl * 2048) >> 4), HI, idPV,
+                                 (first && hl == 0) ? 0u : 1u, bar1, bar2);
         };
         auto tS = [&](uint32_t gs) { return tmem + ((gs & 1) ? C::COL_S1 : C::COL_S0); };
         int use = 0, tau = 0;
@@ -262,10 +338,8 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             if (ok) ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
             if (!ok) break;
             tc_fence_after();
-            issue_s(tS(g), sQt, sRing + (use % C::NS) * C::KVTILE);
-            tc_commit_elect(barS + 8u * (g & 1));
+            issue_s_commit2(tS(g), sQt, sRing + (use % C::NS) * C::KVTILE, barS + 8u * (g & 1), bar_empty(use % C::NS));
             if (u.nk == 1) tc_commit_elect(bar_qfree(buf));
-            tc_commit_elect(bar_empty(use % C::NS));
             ++use;
             for (int j = 0; j < u.nk && ok; ++j) {
                 const uint32_t gs = g + j;
@@ -273,18 +347,15 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                     ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(tS(gs + 1), sQt, sRing + (use % C::NS) * C::KVTILE);
-                    tc_commit_elect(barS + 8u * ((gs + 1) & 1));
+                    issue_s_commit2(tS(gs + 1), sQt, sRing + (use % C::NS) * C::KVTILE, barS + 8u * ((gs + 1) & 1),
+                                    bar_empty(use % C::NS));
                     if (j + 2 == u.nk) tc_commit_elect(bar_qfree(buf));
-                    tc_commit_elect(bar_empty(use % C::NS));
                     ++use;
                 }
                 ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL) && wait_u(barP, gs & 1, S_P);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(tS(gs), sRing + (use % C::NS) * C::KVTILE, j == 0);
-                tc_commit_elect(barPV);
-                tc_commit_elect(bar_empty(use % C::NS));
+                issue_pv_commit2(tS(gs), sRing + (use % C::NS) * C::KVTILE, j == 0, barPV, bar_empty(use % C::NS));
                 ++use;
             }
             g += u.nk;
