@@ -75,8 +75,12 @@ struct Cfg {
     static constexpr int ALLOC_MIN = (D == 64) ? 80 * 1024 : 0;
     static constexpr int ALLOC_RAW = (BYTES + 1024 <= 232448) ? BYTES + 1024 : 232448;
     static constexpr int ALLOC = ALLOC_RAW > ALLOC_MIN ? ALLOC_RAW : ALLOC_MIN;
-    static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN;
-    static constexpr uint32_t TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
+    // D = 256: the query tile also lives in tensor memory (16-bit pairs, D/2 columns), copied in
+    // once per tile, so that the score MMAs read only K from shared memory
+    static constexpr bool QT = (D == 256);
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN, COL_Q = 2 * BN + D;
+    static constexpr uint32_t TMEM_COLS = (2 * BN + D + (QT ? D / 2 : 0) <= 256) ? 256 : 512;
+    static_assert(2 * BN + D + (QT ? D / 2 : 0) <= 512, "tensor-memory columns");
 };
 
 // One probe of a phase by the whole (converged) warp, combined by a warp vote (the fast path of
@@ -130,6 +134,64 @@ __device__ __forceinline__ void mma_s_commit2_elect(uint32_t d_tmem, uint32_t a_
 #undef F1_S_NEXT
 #undef F1_S_HEAD
 #undef F1_S_TAIL
+
+// The query tile into tensor memory: one 128-row x 32-byte copy per 16 columns of D (lane = row,
+// 8 columns of 16-bit pairs each), read from the 128-byte-swizzled, K-major tile that TMA wrote
+// (the same addressing as an MMA A operand), all NP panels behind one elect.sync, then a commit
+// that releases the shared-memory buffer once the copies are done.
+#define F1_CP_STEP(TOFF, SOFF) "add.u32 ta, tq, " #TOFF ";\n\tadd.u32 al, qa, " #SOFF ";\n\t"                   \
+                               "mov.b64 a, {al, %2};\n\t@e tcgen05.cp.cta_group::1.128x256b [ta], a;\n\t"
+#define F1_CP_PANEL "mov.b64 a, {qa, %2};\n\t@e tcgen05.cp.cta_group::1.128x256b [tq], a;\n\t"                  \
+                    F1_CP_STEP(8, 2) F1_CP_STEP(16, 4) F1_CP_STEP(24, 6)
+#define F1_CP_NEXT "add.u32 tq, tq, 32;\n\tadd.u32 qa, qa, %4;\n\t" F1_CP_PANEL
+#define F1_CP_HEAD "{\n\t.reg .b32 tq, qa, ta, al;\n\t.reg .b64 a;\n\t.reg .pred e;\n\t"                      \
+                   "elect.sync _|e, 0xffffffff;\n\tmov.b32 tq, %0;\n\tmov.b32 qa, %1;\n\t" F1_CP_PANEL
+#define F1_CP_TAIL "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%3];\n\t}"
+template <int NP, uint32_t QOFF>
+__device__ __forceinline__ void copy_q_commit_elect(uint32_t t_q, uint32_t q_lo, uint32_t hi, uint32_t bar)
+{
+    static_assert(NP == 2 || NP == 4, "64-column panels of D");
+    if constexpr (NP == 2)
+        asm volatile(F1_CP_HEAD F1_CP_NEXT F1_CP_TAIL ::"r"(t_q), "r"(q_lo), "r"(hi), "r"(bar), "n"(QOFF) : "memory");
+    else
+        asm volatile(F1_CP_HEAD F1_CP_NEXT F1_CP_NEXT F1_CP_NEXT F1_CP_TAIL ::"r"(t_q), "r"(q_lo), "r"(hi), "r"(bar),
+                     "n"(QOFF) : "memory");
+}
+#undef F1_CP_STEP
+#undef F1_CP_PANEL
+#undef F1_CP_NEXT
+#undef F1_CP_HEAD
+#undef F1_CP_TAIL
+
+// S = Q K^T with A = Q from tensor memory (8 columns per 16-column K-step, 32 per panel) and B = K
+// from shared memory, then the two commits (S ready; the K slot released), behind one elect.sync.
+#define F1_T_STEP(TOFF, BOFF) "add.u32 ta, qa, " #TOFF ";\n\tadd.u32 bl, ka, " #BOFF ";\n\t"                  \
+                              "mov.b64 b, {bl, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, t;\n\t"
+#define F1_T_PANEL(ACC) "mov.b64 b, {ka, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [qa], b, %4, " #ACC ";\n\t" \
+                        F1_T_STEP(8, 2) F1_T_STEP(16, 4) F1_T_STEP(24, 6)
+#define F1_T_NEXT "add.u32 qa, qa, 32;\n\tadd.u32 ka, ka, %7;\n\t" F1_T_PANEL(t)
+#define F1_T_HEAD "{\n\t.reg .b32 qa, ka, ta, bl;\n\t.reg .b64 b;\n\t.reg .pred e, f, t;\n\t"                  \
+                  "setp.eq.b32 t, 0, 0;\n\tsetp.ne.b32 f, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"              \
+                  "mov.b32 qa, %1;\n\tmov.b32 ka, %2;\n\t" F1_T_PANEL(f)
+#define F1_T_TAIL "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"            \
+                  "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+template <int NP, uint32_t KOFF>
+__device__ __forceinline__ void mma_s_tq_commit2_elect(uint32_t d_tmem, uint32_t t_q, uint32_t b_lo, uint32_t hi,
+                                                       uint32_t idesc, uint32_t bar1, uint32_t bar2)
+{
+    static_assert(NP == 2 || NP == 4, "64-column panels of D");
+    if constexpr (NP == 2)
+        asm volatile(F1_T_HEAD F1_T_NEXT F1_T_TAIL ::"r"(d_tmem), "r"(t_q), "r"(b_lo), "r"(hi), "r"(idesc),
+                     "r"(bar1), "r"(bar2), "n"(KOFF) : "memory");
+    else
+        asm volatile(F1_T_HEAD F1_T_NEXT F1_T_NEXT F1_T_NEXT F1_T_TAIL ::"r"(d_tmem), "r"(t_q), "r"(b_lo), "r"(hi),
+                     "r"(idesc), "r"(bar1), "r"(bar2), "n"(KOFF) : "memory");
+}
+#undef F1_T_STEP
+#undef F1_T_PANEL
+#undef F1_T_NEXT
+#undef F1_T_HEAD
+#undef F1_T_TAIL
 
 // O += P V over 64 keys (four 16-key steps, as mma_ts_mn4_elect) followed by two commits from
 // the same elected lane (P V done; the V slot released).
@@ -308,8 +370,12 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         // S = Q K^T over D (both K-major, 16 columns of D per instruction), then the commits for
         // S ready and the K slot released, all in one block
         auto issue_s_commit2 = [&](uint32_t dS, uint32_t sQt, uint32_t sK, uint32_t bar1, uint32_t bar2) {
-            mma_s_commit2_elect<D / 64, (uint32_t)C::QPANEL / 16, (uint32_t)C::KVPANEL / 16>(
-                dS, sdesc_lo(sQt, 16), sdesc_lo(sK, 16), HI, idS, bar1, bar2);
+            if constexpr (C::QT)
+                mma_s_tq_commit2_elect<D / 64, (uint32_t)C::KVPANEL / 16>(dS, tmem + C::COL_Q, sdesc_lo(sK, 16), HI,
+                                                                         idS, bar1, bar2);
+            else
+                mma_s_commit2_elect<D / 64, (uint32_t)C::QPANEL / 16, (uint32_t)C::KVPANEL / 16>(
+                    dS, sdesc_lo(sQt, 16), sdesc_lo(sK, 16), HI, idS, bar1, bar2);
         };
         // O += P V over BN keys: A = P from TMEM, B = V (MN-major, 64-column panels C::KVPANEL
         // apart); one group of four 16-key steps per 64 keys, the last group followed by the
@@ -335,11 +401,19 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             ok = wait_u(bar_q(buf), (tau / C::NQ) & 1, S_Q);
             ++tau;
             const uint32_t sQt = sQ + buf * C::QTILE;
+            if constexpr (C::QT) {
+                // The previous tile's score MMAs, the only readers of the query columns, are done:
+                // the softmax read their results before it published the last P waited for above.
+                if (!ok) break;
+                tc_fence_after();
+                copy_q_commit_elect<D / 64, (uint32_t)C::QPANEL / 16>(tmem + C::COL_Q, sdesc_lo(sQt, 16), HI,
+                                                                      bar_qfree(buf));
+            }
             if (ok) ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
             if (!ok) break;
             tc_fence_after();
             issue_s_commit2(tS(g), sQt, sRing + (use % C::NS) * C::KVTILE, barS + 8u * (g & 1), bar_empty(use % C::NS));
-            if (u.nk == 1) tc_commit_elect(bar_qfree(buf));
+            if (!C::QT && u.nk == 1) tc_commit_elect(bar_qfree(buf));
             ++use;
             for (int j = 0; j < u.nk && ok; ++j) {
                 const uint32_t gs = g + j;
@@ -349,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                     tc_fence_after();
                     issue_s_commit2(tS(gs + 1), sQt, sRing + (use % C::NS) * C::KVTILE, barS + 8u * ((gs + 1) & 1),
                                     bar_empty(use % C::NS));
-                    if (j + 2 == u.nk) tc_commit_elect(bar_qfree(buf));
+                    if (!C::QT && j + 2 == u.nk) tc_commit_elect(bar_qfree(buf));
                     ++use;
                 }
                 ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL) && wait_u(barP, gs & 1, S_P);
