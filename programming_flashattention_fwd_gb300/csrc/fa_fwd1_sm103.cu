@@ -20,10 +20,10 @@
 //   warp 2       TMA producer of query tiles (two rotating buffers at D = 128, one at D = 256)
 //   warps 4-7    softmax / lazy correction / epilogue, one thread per query row
 //
-// The softmax consumes every P V completion in order: before publishing P(j) it waits for
-// P V(j-1) (already done in the steady state), so O can be rescaled safely; the epilogue waits
-// for the last one.  Every wait is bounded, as in the main kernel; a CTA that gives up writes
-// NaN into o and lse of every query row it was given.
+// The softmax publishes P(j) as soon as it is written; only a step that rescales O first waits
+// for P V(j-1), and the epilogue waits for the last P V of its tile.  Every wait is bounded, as
+// in the main kernel; a CTA that gives up writes NaN into o and lse of every query row it was
+// given.
 #include <atomic>
 #include <cstdint>
 
@@ -67,7 +67,7 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * QTILE;
     static constexpr int OFF_BAR = OFF_RING + NS * KVTILE;
-    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 1 + 1 + 1;   // q, qfree, full, empty, S[2], P, PV, done
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1;   // q, qfree, full, empty, S[2], P[2], PV[2], done
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     // at D = 64 at least 80 KB, so that no third CTA is co-resident on an SM (two allocations of
@@ -83,13 +83,13 @@ struct Cfg {
     static_assert(2 * BN + D + (QT ? D / 2 : 0) <= 512, "tensor-memory columns");
 };
 
-// One probe of a phase by the whole (converged) warp, combined by a warp vote (the fast path of
-// a warp-uniform wait, without a per-lane branch before the vote).
+// One non-blocking probe of a phase by the whole (converged) warp, combined by a warp vote (the
+// fast path of a warp-uniform wait, without a per-lane branch before the vote).
 __device__ __forceinline__ bool mbar_try_wait_all(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p, q;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "vote.sync.all.pred q, p, 0xffffffff;\n\t"
                  "selp.u32 %0, 1, 0, q;\n\t}"
                  : "=r"(ok)
@@ -259,7 +259,13 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
     auto bar_full = [&](int s) { return bar0 + 8u * (2 * C::NQ + s); };
     auto bar_empty = [&](int s) { return bar0 + 8u * (2 * C::NQ + C::NS + s); };
     const uint32_t barS = bar0 + 8u * (2 * C::NQ + 2 * C::NS);   // + 8 * buffer
-    const uint32_t barP = barS + 16u, barPV = barS + 24u, barDone = barS + 32u;
+    // Key step g signals S ready, P written and P V done on barS / barP / barPV + 8 * (g & 1),
+    // phase (g / 2) & 1.  The softmax publishes P(g + 1) without waiting for P V(g), so it may
+    // run one step ahead of the MMA warp's wait for P(g), and a waiter for P V(g) may have
+    // skipped steps; with two barriers per event neither ever meets a barrier two phases past
+    // the one it waits for (S(g + 2), P(g + 2) and P V(g + 2) all follow the MMA warp's wait
+    // for P(g), which follows the softmax's wait for S(g)).
+    const uint32_t barP = barS + 16u, barPV = barS + 32u, barDone = barS + 48u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     unsigned int *status = &g_fa1_status;
@@ -281,7 +287,9 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         mbar_init(barS, 1);
         mbar_init(barS + 8, 1);
         mbar_init(barP, 4);
+        mbar_init(barP + 8, 4);
         mbar_init(barPV, 1);
+        mbar_init(barPV + 8, 1);
         mbar_init(barDone, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -392,7 +400,7 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         };
         auto tS = [&](uint32_t gs) { return tmem + ((gs & 1) ? C::COL_S1 : C::COL_S0); };
         int use = 0, tau = 0;
-        uint32_t g = 0;   // global key step: S buffer g % 2, barS phase (g / 2) & 1, barP / barPV phase g & 1
+        uint32_t g = 0;   // global key step: S buffer and barS / barP / barPV barrier g % 2, phase (g / 2) & 1
         bool ok = true;
         Unit u;
         for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
@@ -417,19 +425,26 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             ++use;
             for (int j = 0; j < u.nk && ok; ++j) {
                 const uint32_t gs = g + j;
+                // K(j+1) and V(j) (the next two ring slots) are checked before S(j+1) is issued:
+                // its issue blocks while the tensor pipe works through earlier MMAs, and only the
+                // wait for P(j) then stands between it and P V(j)
                 if (j + 1 < u.nk) {
-                    ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
+                    ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL) &&
+                         wait_u(bar_full((use + 1) % C::NS), ((use + 1) / C::NS) & 1, S_FULL);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s_commit2(tS(gs + 1), sQt, sRing + (use % C::NS) * C::KVTILE, barS + 8u * ((gs + 1) & 1),
                                     bar_empty(use % C::NS));
                     if (!C::QT && j + 2 == u.nk) tc_commit_elect(bar_qfree(buf));
                     ++use;
+                } else {
+                    ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
                 }
-                ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL) && wait_u(barP, gs & 1, S_P);
+                ok = ok && wait_u(barP + 8u * (gs & 1), (gs >> 1) & 1, S_P);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv_commit2(tS(gs), sRing + (use % C::NS) * C::KVTILE, j == 0, barPV, bar_empty(use % C::NS));
+                issue_pv_commit2(tS(gs), sRing + (use % C::NS) * C::KVTILE, j == 0, barPV + 8u * (gs & 1),
+                                 bar_empty(use % C::NS));
                 ++use;
             }
             g += u.nk;
@@ -462,7 +477,8 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             for (int j = 0; j < u.nk; ++j) {
                 const uint32_t gs = g + j;
                 const uint32_t tSb = tmem + lane_off + ((gs & 1) ? C::COL_S1 : C::COL_S0);
-                ok = __all_sync(0xffffffffu, bounded_wait(barS + 8u * (gs & 1), (gs >> 1) & 1, abort_flag, tmo, S_S, status));
+                ok = mbar_try_wait_all(barS + 8u * (gs & 1), (gs >> 1) & 1) ||
+                     __all_sync(0xffffffffu, bounded_wait(barS + 8u * (gs & 1), (gs >> 1) & 1, abort_flag, tmo, S_S, status));
                 if (!ok) break;
                 tc_fence_after();
                 // S in 32-column reducing loads: each also returns the maximum of its 32 scores
@@ -528,12 +544,15 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                     }
                     tmem_st_x16(tSb + 16 * c, pk);
                 }
-                // P V(j-1) must be complete before O may be rescaled (and it is consumed here
-                // in every step, keeping the completion count in step with the MMA warp)
-                if (j > 0) {
-                    ok = __all_sync(0xffffffffu, bounded_wait(barPV, (gs - 1) & 1, abort_flag, tmo, S_PV, status));
+                // O may be rescaled only once P V(j-1) is complete; P(j) is published without
+                // that wait otherwise, so that P V(j) can follow P V(j-1) directly.  (S(j) was
+                // issued after P V(j-2), so the barrier of P V(j-1) is at most one phase behind.)
+                if (__any_sync(0xffffffffu, rescale)) {   // only for j > 0
+                    const uint32_t bpv = barPV + 8u * ((gs - 1) & 1), ppv = ((gs - 1) >> 1) & 1;
+                    ok = mbar_try_wait_all(bpv, ppv) ||
+                         __all_sync(0xffffffffu, bounded_wait(bpv, ppv, abort_flag, tmo, S_PV, status));
                     if (!ok) break;
-                    if (__any_sync(0xffffffffu, rescale)) {
+                    {
                         tc_fence_after();
                         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
@@ -556,7 +575,7 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(barP);
+                if (lane == 0) mbar_arrive(barP + 8u * (gs & 1));
                 const uint64_t q0 = f2_add(f2_add(lsum2[0], lsum2[1]), f2_add(lsum2[2], lsum2[3]));
                 const uint64_t q1 = f2_add(f2_add(lsum2[4], lsum2[5]), f2_add(lsum2[6], lsum2[7]));
                 float la, lb;
@@ -565,7 +584,8 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             }
             if (!ok) break;
             // epilogue: the last P V of this tile, then O / l -> 16-bit rows, and the lse
-            ok = __all_sync(0xffffffffu, bounded_wait(barPV, (g + u.nk - 1) & 1, abort_flag, tmo, S_PV, status));
+            const uint32_t gl = g + u.nk - 1;
+            ok = __all_sync(0xffffffffu, bounded_wait(barPV + 8u * (gl & 1), (gl >> 1) & 1, abort_flag, tmo, S_PV, status));
             if (!ok) break;
             g += u.nk;
             tc_fence_after();
