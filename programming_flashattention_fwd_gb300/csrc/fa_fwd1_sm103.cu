@@ -10,9 +10,13 @@
 //   S_0 [0,BN)  S_1 [BN,2BN)   fp32 scores of two consecutive key tiles of BN keys; P (16-bit
 //                              pairs) overwrites the first BN/2 columns of its S
 //   O   [2BN, 2BN+D)           fp32 accumulator
+//   Q   [2BN+D, 2BN+3D/2)      the query tile (16-bit pairs; D >= 128), copied in from shared
+//                              memory by tcgen05.cp at the start of the tile
 // and the MMA warp computes S(j+1) = Q K_{j+1}^T while the softmax works on S(j); then
 // O += P(j) V_j.  Per 64-key step the tensor pipe has 2 x 128*64*D multiply-adds (1024 cycles
-// at D = 256), which the softmax of 64 keys per row fits under.
+// at D = 256), which the softmax of 64 keys per row fits under.  With Q read from tensor memory
+// the score MMAs take only K from shared memory: 64 KB of operand reads per step at D = 256
+// instead of 128 KB, which had held the tensor pipe to about 80 % of its rate.
 //
 //   warp 0       TMA producer of K / V tiles in the order the MMAs consume them (K_0, K_1,
 //                V_0, K_2, V_1, ...), into a ring of BN-row slots
@@ -59,9 +63,9 @@ struct Cfg {
     static constexpr int KVPANEL = BN * 128;       // BN rows of one 64-column panel
     // D = 256: one query buffer and a five-slot K/V ring.  With two query buffers only three
     // 32 KB slots fit, one tile of lookahead, and the MMAs wait for K/V loads (+6 % causal,
-    // +12 % non-causal measured for the deeper ring); the next tile's Q load then starts when
-    // this tile's last S MMA has read its buffer.  D = 128: two query buffers and as many K/V
-    // slots as fit (eight of 16 KB for 64-key steps, five of 32 KB for 128-key steps).
+    // +12 % non-causal measured for the deeper ring).  D = 128: two query buffers and as many
+    // K/V slots as fit (eight of 16 KB for 64-key steps, five of 32 KB for 128-key steps).  From
+    // D = 128 up a query buffer is free again once its tile has been copied into tensor memory.
     static constexpr int NQ = (D == 256) ? 1 : 2;
     static constexpr int NS = (KVTILE_BYTES(D, BN_) == 16384) ? 8 : 5;
     static constexpr int OFF_Q = 0;
@@ -75,9 +79,10 @@ struct Cfg {
     static constexpr int ALLOC_MIN = (D == 64) ? 80 * 1024 : 0;
     static constexpr int ALLOC_RAW = (BYTES + 1024 <= 232448) ? BYTES + 1024 : 232448;
     static constexpr int ALLOC = ALLOC_RAW > ALLOC_MIN ? ALLOC_RAW : ALLOC_MIN;
-    // D = 256: the query tile also lives in tensor memory (16-bit pairs, D/2 columns), copied in
-    // once per tile, so that the score MMAs read only K from shared memory
-    static constexpr bool QT = (D == 256);
+    // D >= 128: the query tile also lives in tensor memory (16-bit pairs, D/2 columns), copied
+    // in once per tile, so that the score MMAs read only K from shared memory (at D = 256 the
+    // operand reads of Q K^T from shared memory otherwise bound the tensor pipe)
+    static constexpr bool QT = (D >= 128);
     static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN, COL_Q = 2 * BN + D;
     static constexpr uint32_t TMEM_COLS = (2 * BN + D + (QT ? D / 2 : 0) <= 256) ? 256 : 512;
     static_assert(2 * BN + D + (QT ? D / 2 : 0) <= 512, "tensor-memory columns");

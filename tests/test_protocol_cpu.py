@@ -1,0 +1,155 @@
+"""Model check of the one-tile kernel's barrier protocol (csrc/fa_fwd1_sm103.cu), on the CPU.
+
+The kernel's MMA warp issues, per key step g of a query tile, S(g + 1) and then P V(g) after
+waiting for P(g); four softmax warps wait for S(g), write P(g) over it and arrive on the P
+barrier, waiting for P V(g - 1) first only when they rescale O; at the end of a tile each
+waits for the tile's last P V.  Every wait is an mbarrier parity wait, which can only tell
+whether the phase of a given parity has completed: a waiter that meets its barrier two phases
+past the phase it wants misreads it.
+
+The model runs the MMA warp, the four softmax warps and an in-order tensor pipe as coroutines
+under random schedules and checks that every wait that passes sees its event really done and
+that the run ends.  Two barriers per event (key step g on barrier g % 2, phase (g / 2) % 2),
+the kernel's scheme, must pass every schedule; one barrier per event is correct only while the
+softmax waits for P V(g - 1) in every step, and fails without that wait.
+"""
+import random
+
+import pytest
+
+
+class _Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.phase = count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def passed(self, parity):
+        # mbarrier.try_wait.parity: true once the phase of this parity has completed, i.e.
+        # while the current phase has the other parity
+        return (self.phase & 1) != parity
+
+
+class _Violation(Exception):
+    pass
+
+
+def _run(seed, two_barriers, wait_pv_every_step, warps=4, plant=None):
+    rnd = random.Random(seed)
+    tiles = [rnd.randint(1, 5) for _ in range(rnd.randint(1, 6))]
+    nb = 2 if two_barriers else 1
+    bar_s = [_Bar(1) for _ in range(2)]            # S buffers alternate in every scheme
+    bar_p = [_Bar(warps) for _ in range(nb)]
+    bar_pv = [_Bar(1) for _ in range(nb)]
+    s_done, pv_done = set(), set()
+    p_done = {w: set() for w in range(warps)}
+    pipe = []
+
+    def pick(bars, g):
+        return bars[g & 1] if len(bars) == 2 else bars[0]
+
+    def parity(bars, g):
+        return ((g >> 1) & 1) if len(bars) == 2 else (g & 1)
+
+    def mma():
+        g = 0
+        for nk in tiles:
+            pipe.append(("S", g))
+            yield
+            for j in range(nk):
+                gs = g + j
+                if j + 1 < nk:
+                    pipe.append(("S", gs + 1))
+                    yield
+                while plant != "mma_skips_p_wait" and not pick(bar_p, gs).passed(parity(bar_p, gs)):
+                    yield "wait"
+                if any(gs not in p_done[w] for w in range(warps)):
+                    raise _Violation(f"MMA warp passed P({gs}) early")
+                pipe.append(("PV", gs))
+                yield
+            g += nk
+
+    def softmax(w):
+        g = 0
+        for nk in tiles:
+            for j in range(nk):
+                gs = g + j
+                while plant != "softmax_skips_s_wait" and not bar_s[gs & 1].passed((gs >> 1) & 1):
+                    yield "wait"
+                if gs not in s_done:
+                    raise _Violation(f"softmax warp {w} passed S({gs}) early")
+                rescale = j > 0 and rnd.random() < 0.3
+                if j > 0 and (rescale or wait_pv_every_step):
+                    while not pick(bar_pv, gs - 1).passed(parity(bar_pv, gs - 1)):
+                        yield "wait"
+                    if gs - 1 not in pv_done:
+                        raise _Violation(f"softmax warp {w} passed P V({gs - 1}) early")
+                p_done[w].add(gs)
+                pick(bar_p, gs).arrive()
+                yield
+            last = g + nk - 1
+            while not pick(bar_pv, last).passed(parity(bar_pv, last)):
+                yield "wait"
+            if last not in pv_done:
+                raise _Violation(f"softmax warp {w} read O before P V({last})")
+            g += nk
+
+    procs = [mma()] + [softmax(w) for w in range(warps)]
+    alive = list(range(len(procs)))
+    idle = 0
+    while alive or pipe:
+        choice = rnd.choice(alive + (["pipe"] if pipe else []))
+        if choice == "pipe":
+            kind, g = pipe.pop(0)   # in order, as the tensor pipe completes them
+            if kind == "S":
+                s_done.add(g)
+                bar_s[g & 1].arrive()
+            else:
+                pv_done.add(g)
+                pick(bar_pv, g).arrive()
+            idle = 0
+            continue
+        try:
+            idle = idle + 1 if next(procs[choice]) == "wait" else 0
+        except StopIteration:
+            alive.remove(choice)
+            idle = 0
+        if idle > 5000:
+            return "deadlock"
+    return "ok"
+
+
+def _outcomes(seeds, **kw):
+    out = {}
+    for seed in range(seeds):
+        try:
+            r = _run(seed, **kw)
+        except _Violation:
+            r = "violation"
+        out[r] = out.get(r, 0) + 1
+    return out
+
+
+def test_two_barriers_per_event_hold_under_every_schedule():
+    """The kernel's scheme: P published without waiting for the previous P V, S / P / P V each
+    on two alternating barriers."""
+    assert _outcomes(600, two_barriers=True, wait_pv_every_step=False) == {"ok": 600}
+
+
+def test_one_barrier_per_event_needs_the_per_step_wait():
+    """With one barrier per event the protocol holds only while every step waits for the
+    previous P V (the softmax cannot then run a step ahead of the MMA warp's wait)."""
+    assert _outcomes(600, two_barriers=False, wait_pv_every_step=True) == {"ok": 600}
+    broken = _outcomes(600, two_barriers=False, wait_pv_every_step=False)
+    assert broken.get("violation", 0) + broken.get("deadlock", 0) > 300
+
+
+@pytest.mark.parametrize("plant", ["softmax_skips_s_wait", "mma_skips_p_wait"])
+def test_model_catches_a_planted_missing_wait(plant):
+    """The checker itself: a role that skips one of its waits is caught on most schedules."""
+    out = _outcomes(200, two_barriers=True, wait_pv_every_step=False, plant=plant)
+    assert out.get("violation", 0) > 100
