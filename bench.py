@@ -64,8 +64,11 @@ PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
 # The default run: the largest single-GPU workload first (the headline of the line), then the
 # other benchmark workloads -- the 4096-token GQA causal one, the non-causal fp16 one with
 # large logits and a ragged tail, the D = 64 causal one and the smallest one.
+# The five benchmark configurations, the largest first (the headline), then the two head-dim-256
+# workloads of the one-query-tile kernel.
 SUITE = ("gqa_causal_b1_h32kv8_s16384", "gqa_causal_b2_h32kv8_s4096", "mha_fp16_b8_h16_s2000_std2",
-         "mha_causal_b4_h16_s1024_d64", "mha_b1_h2_s128_d64")
+         "mha_causal_b4_h16_s1024_d64", "mha_b1_h2_s128_d64",
+         "gqa_causal_b2_h32kv8_s4096_d256", "mha_b4_h16_s2048_d256")
 TARGET_FRAC = 0.60    # of the dense bf16 peak, stated for the D = 128 workloads
 
 

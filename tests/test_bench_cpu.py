@@ -58,8 +58,11 @@ def test_committed_profiles_name_kernel_workload_and_source():
 
 
 def test_suite_leads_with_the_largest_workload():
-    from programming_flashattention_fwd_gb300.inputs import WORKLOADS
-    assert set(bench.SUITE) == set(WORKLOADS)
+    from programming_flashattention_fwd_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS
+    # every benchmark configuration, plus the head-dim-256 workloads, each once
+    assert set(WORKLOADS) <= set(bench.SUITE) <= set(WORKLOADS) | set(EXTRA_WORKLOADS)
+    assert len(set(bench.SUITE)) == len(bench.SUITE)
+    assert any(WORKLOADS.get(n) is None and EXTRA_WORKLOADS[n].D == 256 for n in bench.SUITE)
     head = WORKLOADS[bench.SUITE[0]]
     assert head.flops() == max(w.flops() for w in WORKLOADS.values())
     # the metric's non-causal half is in the suite
