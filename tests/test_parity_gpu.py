@@ -231,6 +231,26 @@ def test_lazy_rescale_threshold(fa, orc, kernel, D):
         assert (l_t - outs[0][1]).abs().max().item() <= 1e-3
 
 
+@pytest.mark.parametrize("dtype,causal,std,tau", [("bf16", 1, 1.0, -1.0), ("bf16", 0, 2.0, -1.0),
+                                                   ("bf16", 2, 2.0, 0.0)])
+def test_one_tile_kernel_several_tiles_per_cta(fa, orc, dtype, causal, std, tau):
+    """D = 256 with 512 query tiles on at most 152 CTAs, so that every CTA runs several tiles in
+    a row: the query copy into tensor memory at each tile start, the score / P / P V barriers
+    whose phases carry on across tiles, and (tau = 0, large logits) a rescale of O at every new
+    row maximum, which waits for the previous P V; every row checked."""
+    w = Workload("several", 2, 16, 4, 2048, 2048, 256, dtype, causal, 4242 + causal, q_std=std, k_std=std)
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full(qd.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd_debug(qd, kd, vd, o, lse, w.causal, w.softmax_scale, kernel=2, tau=tau)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, f"watchdog fired (word {word:#x})"
+    o_ref, l_ref = orc.full(q, k, v, w.is_fp16, causal, w.softmax_scale)
+    check(o, lse, o_ref, l_ref, f"{w} tau {tau}")
+
+
 @pytest.mark.parametrize("kernel,D,dtype,causal,sq,sk", [
     (1, 128, "bf16", 1, 300, 300), (1, 128, "fp16", 0, 257, 300), (1, 64, "bf16", 2, 400, 150),
     (2, 128, "fp16", 1, 300, 300), (2, 256, "bf16", 2, 300, 200), (2, 256, "fp16", 0, 130, 333),
