@@ -142,7 +142,8 @@ int run(const void *q, const void *k, const void *v, void *o, float *lse, int B,
     fa::Maps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (!encode(enc, &maps.q, q, bf16, D, Sq, BHq) || !encode(enc, &maps.k, k, bf16, D, Sk, BHkv, key_tile) ||
-        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv, key_tile) || (kernel == 1 && !encode(enc, &maps.o, o, bf16, D, Sq, BHq)))
+        !encode(enc, &maps.v, v, bf16, D, Sk, BHkv, key_tile) ||
+        ((kernel == 1 || D == 256) && !encode(enc, &maps.o, o, bf16, D, Sq, BHq)))
         return FA_ERR_TENSORMAP;
 
     fa::Params p;

@@ -47,7 +47,9 @@ constexpr int THREADS = 256;
 constexpr uint32_t kNegateA = 1u << 13;  // instruction-descriptor bit: negate A (scale < 0 -> S = -Q K^T)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
-enum Site : uint32_t { S_EMPTY = 1, S_Q = 2, S_FULL = 3, S_P = 4, S_S = 5, S_PV = 6, S_DRAIN = 7, S_QFREE = 8, S_SMEM = 9 };
+enum Site : uint32_t {
+    S_EMPTY = 1, S_Q = 2, S_FULL = 3, S_P = 4, S_S = 5, S_PV = 6, S_DRAIN = 7, S_QFREE = 8, S_SMEM = 9, S_STAGED = 10
+};
 
 // BN keys per step: 64 (the only width at D = 256 whose two score buffers and O fit TMEM; at
 // D = 128 the smaller-tile variant) or 128 (D = 128: the same step as the two-tile kernel).
@@ -71,7 +73,10 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQ * QTILE;
     static constexpr int OFF_BAR = OFF_RING + NS * KVTILE;
-    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1;   // q, qfree, full, empty, S[2], P[2], PV[2], done
+    // D = 256: the finished tile's output rows are staged in the query buffer (free once the next
+    // tile's query tile has been copied into tensor memory) and leave by bulk tensor stores
+    static constexpr bool STAGE_O = (D == 256);
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1 + 3;   // q, qfree, full, empty, S[2], P[2], PV[2], done, qcp, staged[2]
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     // at D = 64 at least 80 KB, so that no third CTA is co-resident on an SM (two allocations of
@@ -84,9 +89,18 @@ struct Cfg {
     // operand reads of Q K^T from shared memory otherwise bound the tensor pipe)
     static constexpr bool QT = (D >= 128);
     static constexpr uint32_t COL_S0 = 0, COL_S1 = BN, COL_O = 2 * BN, COL_Q = 2 * BN + D;
+    static_assert(!STAGE_O || (QT && NQ == 1 && QTILE == BM * D * 2), "O staged in the one query buffer");
     static constexpr uint32_t TMEM_COLS = (2 * BN + D + (QT ? D / 2 : 0) <= 256) ? 256 : 512;
     static_assert(2 * BN + D + (QT ? D / 2 : 0) <= 512, "tensor-memory columns");
 };
+
+// One arrival on `bar` by one elected lane of the (converged) warp.
+__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
 
 // One non-blocking probe of a phase by the whole (converged) warp, combined by a warp vote (the
 // fast path of a warp-uniform wait, without a per-lane branch before the vote).
@@ -247,7 +261,7 @@ constexpr int kMinBlocks = (D == 64) ? 2 : 1;
 template <int D, int KEYS, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
     fa_fwd1_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Params p)
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p)
 {
     using C = Cfg<D, KEYS>;
     constexpr int BN = C::BN;
@@ -271,6 +285,13 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
     // the one it waits for (S(g + 2), P(g + 2) and P V(g + 2) all follow the MMA warp's wait
     // for P(g), which follows the softmax's wait for S(g)).
     const uint32_t barP = barS + 16u, barPV = barS + 32u, barDone = barS + 48u;
+    // With staged output (C::STAGE_O) the one query buffer holds in turn the query tile of tile t
+    // (until its copy into tensor memory completes: barQcp phase t) and the output rows of tile
+    // t - 1 (staged by the softmax warps once Q(t) has been copied: barStaged + 8 * ((t - 1) & 1),
+    // phase ((t - 1) / 2) & 1).  The Q producer writes those rows out with bulk tensor stores and,
+    // once the stores have read them, loads Q(t + 1) into the buffer.  t counts the CTA's tiles
+    // that have keys.
+    const uint32_t barQcp = barS + 56u, barStaged = barS + 64u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     unsigned int *status = &g_fa1_status;
@@ -296,6 +317,9 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         mbar_init(barPV, 1);
         mbar_init(barPV + 8, 1);
         mbar_init(barDone, 1);
+        mbar_init(barQcp, 1);
+        mbar_init(barStaged, 4);
+        mbar_init(barStaged + 8, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -351,13 +375,33 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             int tau = 0;
             const uint64_t once = l2_policy_evict_first();   // each query tile is read once
             bool ok = true;
+            // staged output (C::STAGE_O): tile index and head plane of the last two tiles, whose
+            // rows this thread writes out once their epilogues have staged them
+            int pend_t0 = 0, pend_z0 = 0, pend_t1 = 0, pend_z1 = 0;
+            auto store_o = [&](int k) {
+                if (!bounded_wait(barStaged + 8u * (k & 1), (k >> 1) & 1, abort_flag, tmo, S_STAGED, status))
+                    return false;
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_store_3d(&tmO, pn * 64, ((k & 1) ? pend_t1 : pend_t0) * BM, (k & 1) ? pend_z1 : pend_z0,
+                                 sQ + pn * C::QPANEL);
+                tma_store_commit();
+                tma_store_wait_read();   // the buffer may take the next query tile
+                return true;
+            };
             Unit u;
             for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
                 if (u.nk == 0) continue;
                 const int buf = tau % C::NQ;
-                if (tau >= C::NQ &&
-                    !bounded_wait(bar_qfree(buf), ((tau / C::NQ) - 1) & 1, abort_flag, tmo, S_QFREE, status))
+                if constexpr (C::STAGE_O) {
+                    // Q(1) once Q(0) is in tensor memory; Q(t) for t >= 2 once the rows of tile
+                    // t - 2, staged in the buffer, have been read by their bulk stores
+                    if (tau == 1 && !bounded_wait(barQcp, 0, abort_flag, tmo, S_QFREE, status)) break;
+                    if (tau >= 2 && !store_o(tau - 2)) break;
+                } else if (tau >= C::NQ &&
+                           !bounded_wait(bar_qfree(buf), ((tau / C::NQ) - 1) & 1, abort_flag, tmo, S_QFREE, status)) {
                     break;
+                }
                 mbar_arrive_expect_tx(bar_q(buf), C::QTILE);
                 // scale == 0: every score is 0, so load Q from a plane past the end of the
                 // tensor, which the copy engine fills with zeros
@@ -366,7 +410,19 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                 for (int pn = 0; pn < C::PANELS; ++pn)
                     tma_load_3d_hint(sQ + buf * C::QTILE + pn * C::QPANEL, &tmQ, pn * 64, u.t * BM, zq, bar_q(buf),
                                      once);
+                if (tau & 1) {
+                    pend_t1 = u.t;
+                    pend_z1 = u.zq;
+                } else {
+                    pend_t0 = u.t;
+                    pend_z0 = u.zq;
+                }
                 ++tau;
+            }
+            if constexpr (C::STAGE_O) {
+                // the last two tiles' rows
+                for (int k = max(0, tau - 2); ok && k < tau; ++k) ok = store_o(k);
+                tma_store_wait_all();   // every output store has landed before the CTA exits
             }
             for (int x = max(0, tau - C::NQ); x < tau; ++x)
                 bounded_wait(bar_q(x % C::NQ), (x / C::NQ) & 1, abort_flag, tmo, S_DRAIN, status, false);
@@ -420,7 +476,7 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                 if (!ok) break;
                 tc_fence_after();
                 copy_q_commit_elect<D / 64, (uint32_t)C::QPANEL / 16>(tmem + C::COL_Q, sdesc_lo(sQt, 16), HI,
-                                                                      bar_qfree(buf));
+                                                                      C::STAGE_O ? barQcp : bar_qfree(buf));
             }
             if (ok) ok = wait_u(bar_full(use % C::NS), (use / C::NS) & 1, S_FULL);
             if (!ok) break;
@@ -465,6 +521,7 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         const float sl2 = p.sl2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t g = 0;
+        uint32_t tt = 0;   // tiles with keys finished by this CTA (barQcp, barStaged, bar_qfree phases)
         bool ok = true;
         Unit u;
         for (int round = 0; ok && unit_at<CAUSAL, C::BN>(p, round, u); ++round) {
@@ -596,6 +653,20 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const uint64_t il2 = f2_pack(inv_l, inv_l);
+            if constexpr (C::STAGE_O) {
+                // The query buffer takes this tile's rows once the next tile's query tile (when
+                // this CTA has one) has been copied out of it into tensor memory.
+                bool next = false;
+                {
+                    Unit v;
+                    for (int rr = round + 1; !next && unit_at<CAUSAL, C::BN>(p, rr, v); ++rr) next = v.nk > 0;
+                }
+                if (next) {
+                    ok = mbar_try_wait_all(barQcp, (tt + 1) & 1) ||
+                         __all_sync(0xffffffffu, bounded_wait(barQcp, (tt + 1) & 1, abort_flag, tmo, S_QFREE, status));
+                    if (!ok) break;
+                }
+            }
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t ov[32];
@@ -609,7 +680,15 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                     f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1])), il2), lo, hi);
                     pk[e] = pack2<BF16>(lo, hi);
                 }
-                if (row < p.Sq) {
+                if constexpr (C::STAGE_O) {
+                    // row r of the 64-column panel c / 64, 128B-swizzled as the o tensor map expects
+                    const uint32_t line = sQ + (uint32_t)(c / 64) * C::QPANEL + (uint32_t)r * 128u;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t chunk = (uint32_t)(((c & 63) >> 3) + i) ^ (uint32_t)(r & 7);
+                        st_shared_v4(line + (chunk << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                } else if (row < p.Sq) {
                     if (p.o_al32) {   // full 32-byte sectors: half the store instructions, no partial sectors
                         st_global_v8(orow + c * 2, pk);
                         st_global_v8(orow + c * 2 + 32, pk + 8);
@@ -625,6 +704,15 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                 const float lse = l > 0.f ? (m_used + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
                 p.lse[(size_t)u.zq * p.Sq + row] = lse;
             }
+            if constexpr (C::STAGE_O) {
+                // The rows leave by bulk tensor stores that the Q producer issues (rows >= Sq
+                // clipped by the map), instead of 2*D-byte stores from every thread.  Each writer
+                // makes its rows visible to the copy engine, then each warp arrives.
+                fence_proxy_async_smem();
+                __syncwarp();
+                mbar_arrive_elect(barStaged + 8u * (tt & 1));
+            }
+            ++tt;
         }
     }
 
@@ -668,7 +756,7 @@ static cudaError_t launch_one(const Maps &m, const Params &p, cudaStream_t strea
     // D = 64: one CTA per query tile (two resident per SM), issued heaviest first, so the block
     // scheduler balances the causal tiles of unequal length; otherwise one persistent CTA per SM.
     const int grid = (D == 64) ? p.num_units : min(p.num_units, max(1, sm_count[dev].load(std::memory_order_relaxed)));
-    kern<<<grid, THREADS, Cfg<D, KEYS>::ALLOC, stream>>>(m.q, m.k, m.v, q);
+    kern<<<grid, THREADS, Cfg<D, KEYS>::ALLOC, stream>>>(m.q, m.k, m.v, m.o, q);
     return cudaGetLastError();
 }
 
