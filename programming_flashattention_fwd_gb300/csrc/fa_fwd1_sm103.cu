@@ -21,7 +21,9 @@
 //   warp 0       TMA producer of K / V tiles in the order the MMAs consume them (K_0, K_1,
 //                V_0, K_2, V_1, ...), into a ring of BN-row slots
 //   warp 1       TMEM owner and MMA issuer (whole warp; one elected lane issues)
-//   warp 2       TMA producer of query tiles (two rotating buffers at D = 128, one at D = 256)
+//   warp 2       TMA producer of query tiles (two rotating buffers at D = 128, one at D = 256);
+//                at D = 256 also the bulk tensor stores of each tile's output rows, which the
+//                epilogue stages in the query buffer once the next query tile is in TMEM
 //   warps 4-7    softmax / lazy correction / epilogue, one thread per query row
 //
 // The softmax publishes P(j) as soon as it is written; only a step that rescales O first waits
