@@ -78,7 +78,7 @@ struct Cfg {
     // D = 256: the finished tile's output rows are staged in the query buffer (free once the next
     // tile's query tile has been copied into tensor memory) and leave by bulk tensor stores
     static constexpr bool STAGE_O = (D == 256);
-    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1 + 3;   // q, qfree, full, empty, S[2], P[2], PV[2], done, qcp, staged[2]
+    static constexpr int NBAR = 2 * NQ + 2 * NS + 2 + 2 + 2 + 1 + 4;   // q, qfree, full, empty, S[2], P[2], PV[2], done, qcp, staged[2], oread
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     // at D = 64 at least 80 KB, so that no third CTA is co-resident on an SM (two allocations of
@@ -291,9 +291,10 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
     // (until its copy into tensor memory completes: barQcp phase t) and the output rows of tile
     // t - 1 (staged by the softmax warps once Q(t) has been copied: barStaged + 8 * ((t - 1) & 1),
     // phase ((t - 1) / 2) & 1).  The Q producer writes those rows out with bulk tensor stores and,
-    // once the stores have read them, loads Q(t + 1) into the buffer.  t counts the CTA's tiles
-    // that have keys.
-    const uint32_t barQcp = barS + 56u, barStaged = barS + 64u;
+    // once the stores have read them (barOread phase t - 1), loads Q(t + 1) into the buffer.  The
+    // CTA's last tile has no next query copy to wait for: its epilogue waits for barOread of the
+    // tile before it instead.  t counts the CTA's tiles that have keys.
+    const uint32_t barQcp = barS + 56u, barStaged = barS + 64u, barOread = barS + 80u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     unsigned int *status = &g_fa1_status;
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
         mbar_init(barQcp, 1);
         mbar_init(barStaged, 4);
         mbar_init(barStaged + 8, 4);
+        mbar_init(barOread, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -388,7 +390,8 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                     tma_store_3d(&tmO, pn * 64, ((k & 1) ? pend_t1 : pend_t0) * BM, (k & 1) ? pend_z1 : pend_z0,
                                  sQ + pn * C::QPANEL);
                 tma_store_commit();
-                tma_store_wait_read();   // the buffer may take the next query tile
+                tma_store_wait_read();   // the buffer may take the next query tile, or the last tile's rows
+                mbar_arrive(barOread);
                 return true;
             };
             Unit u;
@@ -666,6 +669,11 @@ __global__ void __launch_bounds__(THREADS, kMinBlocks<D>)
                 if (next) {
                     ok = mbar_try_wait_all(barQcp, (tt + 1) & 1) ||
                          __all_sync(0xffffffffu, bounded_wait(barQcp, (tt + 1) & 1, abort_flag, tmo, S_QFREE, status));
+                    if (!ok) break;
+                } else if (tt >= 1) {
+                    // the last tile: the previous tile's rows must have been read out of the buffer
+                    ok = mbar_try_wait_all(barOread, (tt - 1) & 1) ||
+                         __all_sync(0xffffffffu, bounded_wait(barOread, (tt - 1) & 1, abort_flag, tmo, S_QFREE, status));
                     if (!ok) break;
                 }
             }

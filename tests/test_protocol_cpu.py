@@ -153,3 +153,154 @@ def test_model_catches_a_planted_missing_wait(plant):
     """The checker itself: a role that skips one of its waits is caught on most schedules."""
     out = _outcomes(200, two_barriers=True, wait_pv_every_step=False, plant=plant)
     assert out.get("violation", 0) > 100
+
+
+# ----------------------------------------------------------------------------------------------
+# Staged output at D = 256: the one query buffer holds in turn Q(t) (until its copy into tensor
+# memory completes: barQcp phase t) and the output rows of tile t - 1 (staged by the softmax once
+# Q(t) has been copied: barStaged[(t - 1) % 2]); the Q producer stores those rows, signals that
+# the stores have read them (barOread phase t - 1) and only then loads Q(t + 1).  The last tile
+# has no next query copy to wait for: its epilogue waits for the read of the previous tile's rows
+# instead.  The model checks that no query tile is overwritten before its copy completes, that
+# rows are staged only over a copied query tile or read-out rows, stored only once staged, and
+# never lost.  (A tile's last P V completes after its query copy: the tensor pipe runs them in
+# issue order.)
+
+def _run_staged(seed, two_staged_barriers=True, skip_copy_wait=False, last_waits_read=True):
+    rnd = random.Random(seed)
+    T = rnd.randint(1, 7)
+    bar_q = _Bar(1)                     # Q(t) landed (phase t)
+    bar_qcp = _Bar(1)                   # Q(t) copied into tensor memory (phase t)
+    nst = 2 if two_staged_barriers else 1
+    bar_st = [_Bar(1) for _ in range(nst)]   # rows of tile t staged (one arrival stands for the 4 warps)
+    bar_or = _Bar(1)                    # rows of tile t read by their bulk stores (phase t)
+    buf = {"holds": None}               # ("Q", t) or ("O", t) or None
+    copied, staged, stored = set(), set(), set()
+    inflight = []                       # async completions: ("load", t) / ("copy", t)
+
+    def pick(t):
+        return bar_st[t & 1] if nst == 2 else bar_st[0]
+
+    def par(t):
+        return ((t >> 1) & 1) if nst == 2 else (t & 1)
+
+    def producer():
+        for t in range(T):
+            if t == 1:
+                while not bar_qcp.passed(0):
+                    yield "wait"
+            if t >= 2:
+                k = t - 2
+                while not pick(k).passed(par(k)):
+                    yield "wait"
+                if buf["holds"] != ("O", k):
+                    raise _Violation(f"store of O({k}) finds {buf['holds']}")
+                stored.add(k)
+                buf["holds"] = None                  # the stores have read the buffer
+                bar_or.arrive()
+                yield
+            if buf["holds"] is not None and buf["holds"][0] == "Q" and buf["holds"][1] not in copied:
+                raise _Violation(f"Q({t}) load over an uncopied {buf['holds']}")
+            if buf["holds"] is not None and buf["holds"][0] == "O":
+                raise _Violation(f"Q({t}) load over unstored {buf['holds']}")
+            inflight.append(("load", t))
+            yield
+        for k in range(max(0, T - 2), T):
+            while not pick(k).passed(par(k)):
+                yield "wait"
+            if buf["holds"] != ("O", k):
+                raise _Violation(f"final store of O({k}) finds {buf['holds']}")
+            stored.add(k)
+            buf["holds"] = None
+            bar_or.arrive()
+            yield
+
+    pv_done = set()
+
+    def mma():
+        for t in range(T):
+            while not bar_q.passed(t & 1):
+                yield "wait"
+            if buf["holds"] != ("Q", t):
+                raise _Violation(f"copy of Q({t}) finds {buf['holds']}")
+            inflight.append(("copy", t))
+            yield
+            for _ in range(rnd.randint(0, 3)):       # the tile's key steps
+                yield
+            while t not in copied:                   # in-order pipe: the copy completes first
+                yield "wait"
+            pv_done.add(t)
+
+    def softmax():
+        for t in range(T):
+            while t not in pv_done:
+                yield "wait"
+            if t + 1 < T and not skip_copy_wait:
+                while not bar_qcp.passed((t + 1) & 1):
+                    yield "wait"
+            if t + 1 == T and t >= 1 and last_waits_read:
+                while not bar_or.passed((t - 1) & 1):
+                    yield "wait"
+            h = buf["holds"]
+            if t + 1 < T and h != ("Q", t + 1):
+                raise _Violation(f"O({t}) staged over {h}")
+            if h is not None and h[0] == "Q" and h[1] not in copied:
+                raise _Violation(f"O({t}) staged over uncopied {h}")
+            if h is not None and h[0] == "O":
+                raise _Violation(f"O({t}) staged over unstored {h}")
+            buf["holds"] = ("O", t)
+            staged.add(t)
+            pick(t).arrive()
+            yield
+
+    procs = [producer(), mma(), softmax()]
+    alive = list(range(3))
+    idle = 0
+    while alive or inflight:
+        choice = rnd.choice(alive + (["async"] if inflight else []))
+        if choice == "async":
+            kind, t = inflight.pop(rnd.randrange(len(inflight)))
+            if kind == "load":
+                buf["holds"] = ("Q", t)
+                bar_q.arrive()
+            else:
+                copied.add(t)
+                bar_qcp.arrive()
+            idle = 0
+            continue
+        try:
+            idle = idle + 1 if next(procs[choice]) == "wait" else 0
+        except StopIteration:
+            alive.remove(choice)
+            idle = 0
+        if idle > 5000:
+            return "deadlock"
+    if stored != set(range(T)):
+        raise _Violation("rows lost")
+    return "ok"
+
+
+def _staged_outcomes(seeds, **kw):
+    out = {}
+    for seed in range(seeds):
+        try:
+            r = _run_staged(seed, **kw)
+        except _Violation:
+            r = "violation"
+        out[r] = out.get(r, 0) + 1
+    return out
+
+
+def test_staged_output_protocol_holds():
+    """The kernel's scheme: every query tile copied before the buffer is reused, every tile's
+    rows staged over a copied query tile and stored exactly once, under every schedule."""
+    assert _staged_outcomes(800) == {"ok": 800}
+
+
+def test_staged_output_protocol_catches_planted_mistakes():
+    """Staging without waiting for the next query tile's copy, or the last tile staging without
+    waiting for the previous tile's rows to be read out, each fail."""
+    nowait = _staged_outcomes(800, skip_copy_wait=True)
+    assert nowait.get("violation", 0) > 100
+    noread = _staged_outcomes(800, last_waits_read=False)
+    assert noread.get("violation", 0) > 100
