@@ -181,6 +181,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int r = threadIdx.x - 128;                      // accumulator row == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        // Full 32-byte sectors when every row of C starts on 32 bytes (c aligned, row pitch a
+        // multiple of 32 bytes): half the store instructions of 16-byte stores, no partial sectors.
+        const bool al32 = ((reinterpret_cast<uintptr_t>(p.c) & 31u) == 0) && (p.N % (OUT_F32 ? 8 : 16) == 0);
         int lt = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += G, ++lt) {
@@ -216,7 +219,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                         h[e] = 0.5f * x * (1.f + tanh_approx(k0 * fmaf(k1 * x * x, x, x)));
                     }
                 }
-                if (m < p.M) {
+                if (m < p.M && al32) {
+                    if (OUT_F32) {
+                        float *crow = static_cast<float *>(p.c) + (size_t)m * p.N + n0 + c;
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8)
+                            if (n0 + c + 8 * q8 < p.N) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(h[8 * q8 + e]);
+                                st_global_v8(crow + 8 * q8, w);
+                            }
+                    } else {
+                        uint16_t *crow = static_cast<uint16_t *>(p.c) + (size_t)m * p.N + n0 + c;
+#pragma unroll
+                        for (int q8 = 0; q8 < 2; ++q8)
+                            if (n0 + c + 16 * q8 < p.N) {
+                                uint32_t pk[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) pk[e] = pack2<BF16>(h[16 * q8 + 2 * e], h[16 * q8 + 2 * e + 1]);
+                                st_global_v8(crow + 16 * q8, pk);
+                            }
+                    }
+                } else if (m < p.M) {
                     if (OUT_F32) {
                         float *crow = static_cast<float *>(p.c) + (size_t)m * p.N + n0 + c;
 #pragma unroll
